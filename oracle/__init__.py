@@ -1,0 +1,23 @@
+"""float64 CPU oracle for exact scaled-dot-product attention and paged decode.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU
+baseline leg may import this package; the product library never does, and
+this package imports nothing from the product package.
+
+The arithmetic lives in ``oracle.c`` (plain C, float64, three-pass safe
+softmax per output row); this module only compiles it with gcc and marshals
+numpy / torch CPU arrays into it.
+
+Parity status of each function (the pins live in tests/test_oracle_pins.py):
+  attention      pinned (worked example, closed forms, tiled-vs-naive, mpmath)
+  paged_decode   pinned (equal to attention on the gathered keys; table invariance)
+  decode_elems   pinned (bf16 / e4m3fn codes against torch's conversions)
+"""
+from .oracle import (  # noqa: F401
+    OracleError,
+    attention,
+    build,
+    decode_elems,
+    default_threads,
+    paged_decode,
+)

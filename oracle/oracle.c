@@ -1,0 +1,312 @@
+/*
+ * oracle.c -- float64 CPU oracle for exact scaled-dot-product attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no source, header, table or helper with
+ * the CUDA library and includes nothing from it.
+ *
+ * What it computes (the plain definition, written out, no tiling, no fusion):
+ *
+ *   "FlashAttention V3 实战: Hopper ... Paged KV Cache", section 一 (problem
+ *   definition): Attention(Q,K,V) = softmax(Q K^T / sqrt(d_k)) V.
+ *   "Capstone: CUDA Softmax 与 Attention 算子", section 1.1: the same
+ *   definition, and section 2.1: the row softmax is the three-pass safe
+ *   softmax -- pass 1 m = max_j x_j, pass 2 l = sum_j exp(x_j - m),
+ *   pass 3 p_j = exp(x_j - m) / l.
+ *
+ * For every output row (b, h, i), in float64, on exactly widened inputs:
+ *   s_j = scale * sum_c q_ic k_jc         for j in the row's valid key set
+ *   m   = max_j s_j                        (pass 1)
+ *   l   = sum_j exp(s_j - m)               (pass 2)
+ *   p_j = exp(s_j - m) / l;  o_i = sum_j p_j v_j   (pass 3)
+ *   lse = m + ln(l)
+ *
+ * Readings where the pages leave a step open (each is listed in the design
+ * notes with its justification):
+ *   - scale is the caller's value (1/sqrt(d) in every workload), applied to
+ *     the dot product before the softmax;
+ *   - causal masking is the lower-triangular mask, aligned bottom-right when
+ *     Nq != Nk: key j is valid for query i iff j <= i + (Nk - Nq);
+ *   - a row with no valid key has o = 0 and lse = -inf;
+ *   - lse is the natural-log log-sum-exp of the scaled scores;
+ *   - FP8 inputs are decoded e4m3fn codes multiplied by the per-tensor
+ *     descale; no probability quantisation happens here.
+ *
+ * Paged decode ("FlashAttention V3 实战", section 3.2, paged KV cache) is the
+ * same row computation with one query per request, where key t of request r
+ * lives at cache[block_table[r][t / page_size]][t % page_size][h][:].
+ *
+ * Input element types: float64, float32, bfloat16 bit patterns, e4m3fn bit
+ * patterns.  bf16 and e4m3fn are decoded from their bit-level definitions.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F64 = 0, OR_F32 = 1, OR_BF16 = 2, OR_E4M3 = 3 };
+
+enum { OR_OK = 0, OR_BAD_ARG = 1, OR_NO_MEM = 2, OR_BAD_PAGE = 3 };
+
+/* ---- element decoding ------------------------------------------------- */
+
+/* bfloat16: the upper 16 bits of an IEEE-754 binary32. */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP FP8 e4m3fn: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits,
+ * subnormals when the exponent field is 0, no infinities, and the two codes
+ * with all exponent and mantissa bits set (0x7f, 0xff) are NaN. */
+static double e4m3_bits_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 15;
+    int mant = b & 7;
+    double mag;
+    if (e == 15 && mant == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)mant / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)mant / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+static int dtype_ok(int dt) { return dt == OR_F64 || dt == OR_F32 || dt == OR_BF16 || dt == OR_E4M3; }
+
+/* Widen n consecutive elements starting at element index `off` into out[]. */
+static void load_row(const void* base, int dt, int64_t off, int n, double descale, double* out) {
+    int c;
+    switch (dt) {
+    case OR_F64: {
+        const double* p = (const double*)base + off;
+        for (c = 0; c < n; ++c) out[c] = p[c] * descale;
+    } break;
+    case OR_F32: {
+        const float* p = (const float*)base + off;
+        for (c = 0; c < n; ++c) out[c] = (double)p[c] * descale;
+    } break;
+    case OR_BF16: {
+        const uint16_t* p = (const uint16_t*)base + off;
+        for (c = 0; c < n; ++c) out[c] = bf16_bits_to_double(p[c]) * descale;
+    } break;
+    default: {
+        const uint8_t* p = (const uint8_t*)base + off;
+        for (c = 0; c < n; ++c) out[c] = e4m3_bits_to_double(p[c]) * descale;
+    } break;
+    }
+}
+
+int oracle_decode(const void* src, int dt, int64_t n, double* out) {
+    if (!src || !out || !dtype_ok(dt) || n < 0) return OR_BAD_ARG;
+    for (int64_t i = 0; i < n; i += 4096) {
+        int64_t cnt = n - i < 4096 ? n - i : 4096;
+        load_row(src, dt, i, (int)cnt, 1.0, out + i);
+    }
+    return OR_OK;
+}
+
+/* ---- one output row: the three-pass safe softmax ---------------------- */
+
+typedef struct {
+    const void* k; int k_dt; double k_ds;
+    const void* v; int v_dt; double v_ds;
+    int d;
+    double scale;
+} kv_src;
+
+/* key_off[j] = element offset of key j's row (same offset indexes K and V).
+ * qrow: the widened query row.  s: scratch of n doubles; kr: scratch of d. */
+static void attend_row(const kv_src* src, const double* qrow, const int64_t* key_off, int64_t n,
+                       double* s, double* kr, double* o, double* lse, double* psum) {
+    const int d = src->d;
+    int64_t j;
+    int c;
+    for (c = 0; c < d; ++c) o[c] = 0.0;
+    if (n <= 0) {
+        *lse = -INFINITY;
+        if (psum) *psum = 0.0;
+        return;
+    }
+    /* scores */
+    for (j = 0; j < n; ++j) {
+        double acc = 0.0;
+        load_row(src->k, src->k_dt, key_off[j], d, src->k_ds, kr);
+        for (c = 0; c < d; ++c) acc += qrow[c] * kr[c];
+        s[j] = src->scale * acc;
+    }
+    /* pass 1: the row maximum */
+    double m = s[0];
+    for (j = 1; j < n; ++j)
+        if (s[j] > m) m = s[j];
+    /* pass 2: the denominator */
+    double l = 0.0;
+    for (j = 0; j < n; ++j) l += exp(s[j] - m);
+    /* pass 3: probabilities and the weighted sum of value rows */
+    double ps = 0.0;
+    for (j = 0; j < n; ++j) {
+        double p = exp(s[j] - m) / l;
+        ps += p;
+        load_row(src->v, src->v_dt, key_off[j], d, src->v_ds, kr);
+        for (c = 0; c < d; ++c) o[c] += p * kr[c];
+    }
+    *lse = m + log(l);
+    if (psum) *psum = ps;
+}
+
+/* ---- threading: rows are handed out one at a time from a shared counter */
+
+typedef struct {
+    /* dense problem */
+    const void* q; int q_dt; double q_ds;
+    kv_src kv;
+    int64_t BH, Nq, Nk;
+    int causal;
+    const int64_t* rows; int64_t n_rows;
+    /* paged problem (used when paged != 0) */
+    int paged;
+    const int32_t* block_table; const int32_t* seq_lens;
+    int H, page_size, max_pages; int64_t num_pages;
+    /* outputs */
+    double* o; double* lse; double* psum;
+    /* work distribution and error reporting */
+    int64_t next;
+    int err;
+} job_t;
+
+static void* worker(void* arg) {
+    job_t* jb = (job_t*)arg;
+    const int d = jb->kv.d;
+    int64_t nk_max = jb->paged ? (int64_t)jb->max_pages * jb->page_size : jb->Nk;
+    if (nk_max < 1) nk_max = 1;
+    double* s = (double*)malloc(sizeof(double) * nk_max);
+    int64_t* off = (int64_t*)malloc(sizeof(int64_t) * nk_max);
+    double* kr = (double*)malloc(sizeof(double) * d);
+    double* qr = (double*)malloc(sizeof(double) * d);
+    if (!s || !off || !kr || !qr) {
+        __atomic_store_n(&jb->err, OR_NO_MEM, __ATOMIC_RELAXED);
+        free(s); free(off); free(kr); free(qr);
+        return NULL;
+    }
+    for (;;) {
+        int64_t r = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (r >= jb->n_rows) break;
+        int64_t n = 0, j;
+        if (!jb->paged) {
+            int64_t row = jb->rows ? jb->rows[r] : r; /* flattened (bh, i) */
+            int64_t bh = row / jb->Nq, i = row % jb->Nq;
+            load_row(jb->q, jb->q_dt, row * d, d, jb->q_ds, qr);
+            n = jb->Nk;
+            if (jb->causal) {
+                int64_t last = i + (jb->Nk - jb->Nq); /* bottom-right aligned */
+                n = last + 1;
+                if (n < 0) n = 0;
+                if (n > jb->Nk) n = jb->Nk;
+            }
+            for (j = 0; j < n; ++j) off[j] = (bh * jb->Nk + j) * d;
+        } else {
+            int64_t req = r / jb->H, h = r % jb->H;
+            load_row(jb->q, jb->q_dt, r * d, d, jb->q_ds, qr);
+            n = jb->seq_lens[req];
+            if (n < 0 || n > (int64_t)jb->max_pages * jb->page_size) {
+                __atomic_store_n(&jb->err, OR_BAD_PAGE, __ATOMIC_RELAXED);
+                n = 0;
+            }
+            for (j = 0; j < n; ++j) {
+                int64_t page = jb->block_table[req * jb->max_pages + j / jb->page_size];
+                if (page < 0 || page >= jb->num_pages) {
+                    __atomic_store_n(&jb->err, OR_BAD_PAGE, __ATOMIC_RELAXED);
+                    n = 0;
+                    break;
+                }
+                off[j] = ((page * jb->page_size + j % jb->page_size) * jb->H + h) * d;
+            }
+        }
+        attend_row(&jb->kv, qr, off, n, s, kr, jb->o + r * d, jb->lse + r,
+                   jb->psum ? jb->psum + r : NULL);
+    }
+    free(s); free(off); free(kr); free(qr);
+    return NULL;
+}
+
+static int run_job(job_t* jb, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    if ((int64_t)nthreads > jb->n_rows) nthreads = jb->n_rows > 0 ? (int)jb->n_rows : 1;
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+    if (!th) return OR_NO_MEM;
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, worker, jb) != 0) break;
+        ++started;
+    }
+    if (started == 0) worker(jb); /* no thread could be created: run inline */
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    free(th);
+    return jb->err;
+}
+
+/* Dense attention over BHSD-contiguous tensors.
+ *   q: [BH, Nq, d], k and v: [BH, Nk, d], element types q_dt / k_dt / v_dt,
+ *   each element multiplied by its tensor's descale (1.0 for bf16/f32/f64).
+ *   rows: optional list of flattened row ids bh*Nq + i (NULL = all rows in
+ *   order).  o: [n_rows, d], lse: [n_rows], psum (optional): [n_rows], the sum
+ *   of the row's probabilities as computed in pass 3. */
+int oracle_attention(const void* q, int q_dt, double q_ds,
+                     const void* k, int k_dt, double k_ds,
+                     const void* v, int v_dt, double v_ds,
+                     int64_t BH, int64_t Nq, int64_t Nk, int d, double scale, int causal,
+                     const int64_t* rows, int64_t n_rows,
+                     double* o, double* lse, double* psum, int nthreads) {
+    if (!q || !k || !v || !o || !lse) return OR_BAD_ARG;
+    if (!dtype_ok(q_dt) || !dtype_ok(k_dt) || !dtype_ok(v_dt)) return OR_BAD_ARG;
+    if (BH < 0 || Nq < 0 || Nk < 0 || d < 1 || d > 4096) return OR_BAD_ARG;
+    if (!rows) n_rows = BH * Nq;
+    if (n_rows < 0) return OR_BAD_ARG;
+    if (rows)
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= BH * Nq) return OR_BAD_ARG;
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.q_dt = q_dt; jb.q_ds = q_ds;
+    jb.kv.k = k; jb.kv.k_dt = k_dt; jb.kv.k_ds = k_ds;
+    jb.kv.v = v; jb.kv.v_dt = v_dt; jb.kv.v_ds = v_ds;
+    jb.kv.d = d; jb.kv.scale = scale;
+    jb.BH = BH; jb.Nq = Nq; jb.Nk = Nk; jb.causal = causal;
+    jb.rows = rows; jb.n_rows = n_rows;
+    jb.o = o; jb.lse = lse; jb.psum = psum;
+    return run_job(&jb, nthreads);
+}
+
+/* Paged-KV decode: one query token per request.
+ *   q: [B, H, d]; k_cache and v_cache: [num_pages, page_size, H, d];
+ *   block_table: [B, max_pages] physical page ids; seq_lens: [B].
+ *   o: [B*H, d], lse: [B*H], psum optional [B*H].  Returns OR_BAD_PAGE (and
+ *   treats the row as empty) when a length or a page id needed by a row is
+ *   out of range. */
+int oracle_paged_decode(const void* q, int q_dt,
+                        const void* k_cache, const void* v_cache, int kv_dt,
+                        const int32_t* block_table, const int32_t* seq_lens,
+                        int B, int H, int d, int page_size, int max_pages, int64_t num_pages,
+                        double scale, double* o, double* lse, double* psum, int nthreads) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse) return OR_BAD_ARG;
+    if (!dtype_ok(q_dt) || !dtype_ok(kv_dt)) return OR_BAD_ARG;
+    if (B < 0 || H < 1 || d < 1 || d > 4096 || page_size < 1 || max_pages < 0 || num_pages < 0)
+        return OR_BAD_ARG;
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.q_dt = q_dt; jb.q_ds = 1.0;
+    jb.kv.k = k_cache; jb.kv.k_dt = kv_dt; jb.kv.k_ds = 1.0;
+    jb.kv.v = v_cache; jb.kv.v_dt = kv_dt; jb.kv.v_ds = 1.0;
+    jb.kv.d = d; jb.kv.scale = scale;
+    jb.paged = 1;
+    jb.block_table = block_table; jb.seq_lens = seq_lens;
+    jb.H = H; jb.page_size = page_size; jb.max_pages = max_pages; jb.num_pages = num_pages;
+    jb.n_rows = (int64_t)B * H;
+    jb.o = o; jb.lse = lse; jb.psum = psum;
+    return run_job(&jb, nthreads);
+}
