@@ -1,1 +1,224 @@
-"""GB300-native exact attention: placeholder, replaced by the ctypes binding."""
+"""GB300-native (sm_103a) exact attention: Python binding of the C ABI in include/attn.h.
+
+Argument marshalling only.  Every step of attention runs in the CUDA library
+``libattn_gb300.so`` built in-tree from ``csrc/``; there is no CPU or
+PyTorch fallback, and every call raises if the library is missing.
+
+Two levels:
+  * ``attn_fwd``, ``attn_fwd_fp8``, ``attn_paged_decode``,
+    ``attn_paged_decode_workspace_size``, ``attn_device_status``,
+    ``attn_status_string``: the C entry points, same names and argument
+    order, taking raw device pointers (ints) and a stream handle (int).
+  * ``fwd``, ``fwd_fp8``, ``paged_decode``: take torch CUDA tensors, allocate
+    outputs with torch when none are given, call the C entry point on the
+    current stream and raise ``AttnError`` on a non-zero status.
+"""
+import ctypes
+import math
+import os
+import threading
+
+from . import inputs  # noqa: F401  (seeded synthetic input recipes)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn_gb300.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_WORKSPACE = 4
+ATTN_ERR_TIMEOUT = 5
+ATTN_ERR_DEVICE_DATA = 6
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (what or "attn", attn_status_string(status), status))
+
+
+def build(force=False):
+    """Compile the CUDA library in-tree (nvcc, sm_103a) and load it."""
+    from . import _build
+    _build.build(force=force)
+    global _lib
+    with _lock:
+        _lib = None
+    return lib()
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("CUDA library %s is missing: build it with "
+                                   "attention_attn_fwd_03_gb300.build() (nvcc, sm_103a)" % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.attn_fwd.restype = i
+            L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+            L.attn_fwd_fp8.restype = i
+            L.attn_fwd_fp8.argtypes = [vp, vp, vp, f, f, f, vp, vp, i, i, i, i, i, f, i, vp]
+            L.attn_paged_decode_workspace_size.restype = sz
+            L.attn_paged_decode_workspace_size.argtypes = [i, i, i, i, i]
+            L.attn_paged_decode.restype = i
+            L.attn_paged_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
+            L.attn_device_status.restype = i
+            L.attn_device_status.argtypes = [vp]
+            L.attn_status_string.restype = ctypes.c_char_p
+            L.attn_status_string.argtypes = [i]
+            _lib = L
+        return _lib
+
+
+# ---------------------------------------------------------------- C entry points
+
+def attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream):
+    return lib().attn_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream)
+
+
+def attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, Nq, Nk, d, scale, causal, stream):
+    return lib().attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, Nq, Nk, d, scale,
+                              causal, stream)
+
+
+def attn_paged_decode_workspace_size(B, H, d, page_size, max_pages_per_seq):
+    return lib().attn_paged_decode_workspace_size(B, H, d, page_size, max_pages_per_seq)
+
+
+def attn_paged_decode(q, k_cache, v_cache, block_table, seq_lens, B, H, d, page_size, max_pages_per_seq,
+                      num_pages, scale, o, lse, workspace, workspace_bytes, stream):
+    return lib().attn_paged_decode(q, k_cache, v_cache, block_table, seq_lens, B, H, d, page_size,
+                                   max_pages_per_seq, num_pages, scale, o, lse, workspace, workspace_bytes,
+                                   stream)
+
+
+def attn_device_status(stream):
+    return lib().attn_device_status(stream)
+
+
+def attn_status_string(status):
+    return lib().attn_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- torch helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _check(t, name, dtype, shape=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def _raise(st, what):
+    if st != ATTN_OK:
+        raise AttnError(st, what)
+
+
+def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, stream=None):
+    """bf16 [B,H,Nq,d] / [B,H,Nk,d] -> (o bf16 [B,H,Nq,d], lse fp32 [B,H,Nq])."""
+    torch = _torch()
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16, (B, H, Nk, d))
+    _check(v, "v", torch.bfloat16, (B, H, Nk, d))
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, q.shape)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (B, H, Nq))
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                  lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, sc, int(bool(causal)),
+                  _stream(stream))
+    _raise(st, "attn_fwd")
+    return out, lse
+
+
+def fwd_fp8(q8, k8, v8, descales, causal=False, scale=None, out=None, lse=None, return_lse=True, stream=None):
+    """e4m3fn [B,H,N,d] with per-tensor descales (q, k, v) -> (o bf16, lse fp32)."""
+    torch = _torch()
+    B, H, Nq, d = q8.shape
+    Nk = k8.shape[2]
+    _check(q8, "q8", torch.float8_e4m3fn)
+    _check(k8, "k8", torch.float8_e4m3fn, (B, H, Nk, d))
+    _check(v8, "v8", torch.float8_e4m3fn, (B, H, Nk, d))
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q8.device)
+    _check(out, "out", torch.bfloat16, (B, H, Nq, d))
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q8.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (B, H, Nq))
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    dq, dk, dv = (float(x) for x in descales)
+    st = attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), dq, dk, dv, out.data_ptr(),
+                      lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, sc, int(bool(causal)),
+                      _stream(stream))
+    _raise(st, "attn_fwd_fp8")
+    return out, lse
+
+
+def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, out=None, lse=None, workspace=None,
+                 return_lse=True, stream=None):
+    """q bf16 [B,H,d]; caches bf16 [num_pages, page_size, H, d]; block_table int32
+    [B, max_pages]; seq_lens int32 [B] -> (o bf16 [B,H,d], lse fp32 [B,H])."""
+    torch = _torch()
+    B, H, d = q.shape
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    max_pages = block_table.shape[1]
+    _check(q, "q", torch.bfloat16)
+    _check(k_cache, "k_cache", torch.bfloat16, (num_pages, page_size, H, d))
+    _check(v_cache, "v_cache", torch.bfloat16, (num_pages, page_size, H, d))
+    _check(block_table, "block_table", torch.int32, (B, max_pages))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, (B, H, d))
+    if lse is None and return_lse:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (B, H))
+    ws_bytes = attn_paged_decode_workspace_size(B, H, d, page_size, max_pages)
+    if ws_bytes == 0:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "attn_paged_decode_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    st = attn_paged_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                           seq_lens.data_ptr(), B, H, d, page_size, max_pages, num_pages, sc, out.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, workspace.data_ptr(), workspace.numel(),
+                           _stream(stream))
+    _raise(st, "attn_paged_decode")
+    return out, lse
+
+
+def device_status(stream=None):
+    """Synchronise and raise AttnError if a kernel flagged a timeout or bad device data."""
+    _raise(attn_device_status(_stream(stream)), "attn_device_status")

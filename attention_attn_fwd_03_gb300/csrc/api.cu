@@ -1,0 +1,219 @@
+// api.cu -- the extern "C" entry points declared in include/attn.h.
+//
+// Host-side only: argument validation (nothing is enqueued on a bad
+// argument), TMA tensor-map encoding, per-device cached state (the device
+// status word's address), and the kernel launches.  No allocation happens
+// here or in any kernel.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "attn.h"
+#include "kernels.h"
+
+namespace attn {
+
+// Bit k set <=> a kernel reported status code k (ATTN_ERR_TIMEOUT,
+// ATTN_ERR_DEVICE_DATA).  One word per device; cleared by attn_device_status.
+__device__ unsigned g_status_word;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    unsigned* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+attn_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// Per-device set-up, once: the status word's device address.
+attn_status_t device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& s = g_dev[dev];
+    if (!s.ready) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
+        s.status = static_cast<unsigned*>(ptr);
+        s.ready = true;
+    }
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return ATTN_ERR_CUDA;
+        g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    *out = &s;
+    return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D map over a [BH, rows, d] tensor: box = (128 bytes of d, 128 rows, 1),
+// 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* map, const void* base, bool fp8, int d, long long rows, long long bh) {
+    const int eb = fp8 ? 1 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
+    cuuint64_t strides[2] = {(cuuint64_t)d * eb, (cuuint64_t)rows * d * eb};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / eb), 128u, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+attn_status_t prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                      int Nk, int d, float scale, int causal, bool fp8, float dq, float dk, float dv,
+                      void* stream) {
+    if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (fp8 && !(std::isfinite(dq) && dq > 0.f && std::isfinite(dk) && dk > 0.f && std::isfinite(dv) && dv > 0.f))
+        return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if (fp8 ? d != 128 : (d != 64 && d != 128)) return ATTN_ERR_UNSUPPORTED;
+
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+
+    const long long BH = (long long)B * H;
+    PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    if (!make_map(&p.tm_q, q, fp8, d, Nq, BH) || !make_map(&p.tm_k, k, fp8, d, Nk, BH) ||
+        !make_map(&p.tm_v, v, fp8, d, Nk, BH) || !make_map(&p.tm_o, o, false, d, Nq, BH))
+        return ATTN_ERR_CUDA;
+    p.lse = lse;
+    p.status = ds->status;
+    p.BH = (int)BH;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.causal = causal;
+    p.n_pairs = (Nq + 255) / 256;
+    const float log2e = 1.4426950408889634f;
+    p.c_scale = fp8 ? scale * dq * dk * log2e : scale * log2e;
+    p.o_scale = fp8 ? dv : 1.f;
+    const long long grid = (long long)p.n_pairs * BH;
+    if (grid > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    return from_cuda(launch_prefill(d, fp8, p, (int)grid, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                       int Nk, int d, float scale, int causal, void* stream) {
+    return prefill(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, false, 1.f, 1.f, 1.f, stream);
+}
+
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float q_descale, float k_descale,
+                           float v_descale, void* o, float* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                           int causal, void* stream) {
+    return prefill(q8, k8, v8, o, lse, B, H, Nq, Nk, d, scale, causal, true, q_descale, k_descale, v_descale,
+                   stream);
+}
+
+size_t attn_paged_decode_workspace_size(int B, int H, int d, int page_size, int max_pages_per_seq) {
+    if (B < 1 || H < 1 || (d != 64 && d != 128) || page_size < 8 || page_size > 1024 || page_size % 8 != 0 ||
+        max_pages_per_seq < 1)
+        return 0;
+    return decode_plan(B, H, d, page_size, max_pages_per_seq).workspace_bytes;
+}
+
+attn_status_t attn_paged_decode(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                                const int32_t* seq_lens, int B, int H, int d, int page_size, int max_pages_per_seq,
+                                int num_pages, float scale, void* o, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || max_pages_per_seq < 1 || num_pages < 1 || page_size < 1) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || page_size < 8 || page_size > 1024 || page_size % 8 != 0)
+        return ATTN_ERR_UNSUPPORTED;
+    if ((long long)max_pages_per_seq * page_size > 0x7fffffffLL || (long long)B * max_pages_per_seq > 0x7fffffffLL)
+        return ATTN_ERR_INVALID_ARG;
+    const DecodePlan pl = decode_plan(B, H, d, page_size, max_pages_per_seq);
+    if (!workspace || workspace_bytes < pl.workspace_bytes || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+    if (pl.max_splits > 65535 || B > 65535) return ATTN_ERR_UNSUPPORTED;
+
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+
+    DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = static_cast<const uint16_t*>(q);
+    p.k_cache = static_cast<const uint16_t*>(k_cache);
+    p.v_cache = static_cast<const uint16_t*>(v_cache);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.part_o = static_cast<float*>(workspace);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + (pl.workspace_bytes - pl.part_ml_bytes));
+    p.o = static_cast<uint16_t*>(o);
+    p.lse = lse;
+    p.status = ds->status;
+    p.B = B;
+    p.H = H;
+    p.page_size = page_size;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.pages_per_split = pl.pages_per_split;
+    p.max_splits = pl.max_splits;
+    p.c_scale = scale * 1.4426950408889634f;
+    return from_cuda(launch_paged_decode(d, p, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_device_status(void* stream) {
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof word) != cudaSuccess) return ATTN_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (word & (1u << ATTN_ERR_TIMEOUT)) return ATTN_ERR_TIMEOUT;
+    if (word & (1u << ATTN_ERR_DEVICE_DATA)) return ATTN_ERR_DEVICE_DATA;
+    return ATTN_OK;
+}
+
+const char* attn_status_string(attn_status_t s) {
+    switch (s) {
+    case ATTN_OK: return "success";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA runtime or launch failure";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case ATTN_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+    case ATTN_ERR_DEVICE_DATA: return "device-side length or page id out of range";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Throughput benchmark of the GB300 attention library.
+
+One step = one pass of the prefill hot path over the batched workload
+(B=4, H=16, Nq=Nk=2048, d=128, bf16): attn_fwd non-causal, then attn_fwd
+causal, on inputs already resident in HBM.  The headline metric is TFLOPS
+with the algorithmic count 4*B*H*Nq*Nk*d per call (halved for the causal
+call).  Inputs (100 MB) are smaller than L2, so L2 is flushed (a 256 MB
+write) before every timed step, outside the timed events.
+
+Also reported in the same JSON line (timed the same way, not part of
+`value`): the long causal prefill (1x32x32768, d=128), FP8 prefill
+(2x16x8192, d=128) and paged decode (64 requests, H=32, d=128, 64-token
+pages) -- the latter as HBM GB/s of algorithmic bytes.
+
+`--impl reference` times the float64 CPU oracle (the only reference this
+method has) on a bounded row sample of the same workload.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica of
+the step on its own inputs (weak scaling, no data-path collective); the
+elapsed time is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+B, H, N, D = 4, 16, 2048, 128
+WORKLOAD = "batched prefill B=4 H=16 Nq=Nk=2048 d=128 bf16, non-causal + causal per step"
+METRIC = "attention fwd TFLOPS and % of GB300 tensor peak; paged decode HBM GB/s"
+
+
+def prefill_flops(b, h, nq, nk, d, causal):
+    f = 4.0 * b * h * nq * nk * d
+    return f / 2 if causal else f
+
+
+STEP_FLOPS = prefill_flops(B, H, N, N, D, False) + prefill_flops(B, H, N, N, D, True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in (out or "").splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- timing helpers
+
+def timed_launches(torch, fn, iters, flush):
+    """Run fn() `iters` times, flushing L2 before each; returns per-call ms (CUDA events)."""
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(iters):
+        flush()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return times
+
+
+def traffic_record(kernel_file, key):
+    """DRAM bytes per launch from a committed ncu summary, valid only while the
+    kernel source is unchanged (sha256 recorded at capture time)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[key]
+        with open(os.path.join(ROOT, "attention_attn_fwd_03_gb300", "csrc", kernel_file), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        if rec.get("source_sha256") != sha:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import attention_attn_fwd_03_gb300 as attn
+    from attention_attn_fwd_03_gb300 import inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    attn.lib()
+    peaks = load_peaks()
+
+    flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    # inputs: seeded per rank (each rank is an independent replica)
+    q, k, v = (t.to(dev) for t in inputs.dense_qkv(B, H, N, N, D, seed=rank))
+    o_nc, l_nc = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    o_c, l_c = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+    def step():
+        attn.fwd(q, k, v, causal=False, out=o_nc, lse=l_nc)
+        attn.fwd(q, k, v, causal=True, out=o_c, lse=l_c)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    attn.device_status()
+
+    # per-launch durations of the dominant kernel (the prefill kernel, both calls)
+    nc_ms = timed_launches(torch, lambda: attn.fwd(q, k, v, causal=False, out=o_nc, lse=l_nc), 5, flush)
+    c_ms = timed_launches(torch, lambda: attn.fwd(q, k, v, causal=True, out=o_c, lse=l_c), 5, flush)
+
+    # ---- timed region: exactly K steps
+    stream = torch.cuda.current_stream()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(args.steps):
+            flush()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    attn.device_status()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = STEP_FLOPS * world * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API from pinned host buffers
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty((2, B, H, N, D), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((2, B, H, N), dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        attn.fwd(dq, dk, dv, causal=False, out=o_nc, lse=l_nc)
+        attn.fwd(dq, dk, dv, causal=True, out=o_c, lse=l_c)
+        ho[0].copy_(o_nc, non_blocking=True)
+        ho[1].copy_(o_c, non_blocking=True)
+        hl[0].copy_(l_nc, non_blocking=True)
+        hl[1].copy_(l_c, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_ms = timed_launches(torch, e2e_step, max(3, min(args.steps, 10)), flush)
+    h2d = 3 * q.numel() * 2
+    d2h = 2 * (o_nc.numel() * 2 + l_nc.numel() * 4)
+    e2e_val = STEP_FLOPS / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+
+    # ---- dominant kernel roofline (prefill kernel: both calls of the step)
+    launch_flops = prefill_flops(B, H, N, N, D, False) + prefill_flops(B, H, N, N, D, True)
+    launch_ms = statistics.mean(nc_ms) + statistics.mean(c_ms)
+    achieved = launch_flops / (launch_ms * 1e-3) / 1e12
+    traffic_nc = traffic_record("prefill.cu", "prefill_bf16_d128_batched_noncausal")
+    traffic_c = traffic_record("prefill.cu", "prefill_bf16_d128_batched_causal")
+    traffic = (traffic_nc + traffic_c) / 2 if (traffic_nc is not None and traffic_c is not None) else None
+
+    secondary = {}
+    if not args.no_secondary:
+        secondary = run_secondary(torch, attn, inputs, dev, flush, peaks, rank)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), rounded to bf16)",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D,
+                   "calls_per_step": ["non-causal", "causal"], "flops_per_step": STEP_FLOPS,
+                   "l2": "flushed (256 MB write) before every timed step, outside the timed events",
+                   "parallelism": "replicas (one independent workload per GPU)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "traffic": traffic, "kernel": "prefill_kernel<128,bf16>",
+                     "peak_source": peaks["source"] + " dense bf16 (burst, kernel timed alone)"},
+        "e2e": {"value": round(e2e_val, 3), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(statistics.mean(e2e_ms), 4)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "per_call_ms": {"non_causal": round(statistics.mean(nc_ms), 4), "causal": round(statistics.mean(c_ms), 4)},
+        "workloads": secondary,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sample_seconds=args.cpu_seconds)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_secondary(torch, attn, inputs, dev, flush, peaks, rank):
+    out = {}
+    reps = 5
+    # long causal prefill
+    q, k, v = (t.to(dev) for t in inputs.dense_qkv(1, 32, 32768, 32768, 128, seed=rank))
+    o, l = torch.empty_like(q), torch.empty((1, 32, 32768), dtype=torch.float32, device=dev)
+    attn.fwd(q, k, v, causal=True, out=o, lse=l)
+    ms = timed_launches(torch, lambda: attn.fwd(q, k, v, causal=True, out=o, lse=l), reps, flush)
+    f = prefill_flops(1, 32, 32768, 32768, 128, True)
+    tf = f / (statistics.mean(ms) * 1e-3) / 1e12
+    out["long_causal_prefill_1x32x32768_d128"] = {
+        "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
+        "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4)}
+    del q, k, v, o, l
+    # FP8 prefill
+    q, k, v = inputs.dense_qkv(2, 16, 8192, 8192, 128, seed=rank)
+    (q8, dq), (k8, dk), (v8, dv) = (inputs.fp8_quantize(t) for t in (q, k, v))
+    q8, k8, v8 = q8.to(dev), k8.to(dev), v8.to(dev)
+    o, l = torch.empty((2, 16, 8192, 128), dtype=torch.bfloat16, device=dev), \
+        torch.empty((2, 16, 8192), dtype=torch.float32, device=dev)
+    attn.fwd_fp8(q8, k8, v8, (dq, dk, dv), out=o, lse=l)
+    ms = timed_launches(torch, lambda: attn.fwd_fp8(q8, k8, v8, (dq, dk, dv), out=o, lse=l), reps, flush)
+    f = prefill_flops(2, 16, 8192, 8192, 128, False)
+    tf = f / (statistics.mean(ms) * 1e-3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    out["fp8_prefill_2x16x8192_d128"] = {
+        "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
+        "frac_of_fp8_peak": round(tf / fp8_peak, 4),
+        "fp8_peak_note": "measured bf16 burst x 2 (nominal fp8:bf16 dense ratio)"}
+    del q, k, v, q8, k8, v8, o, l
+    # paged decode
+    p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
+                        len_hi=8192, seed=rank, device=dev)
+    o = torch.empty_like(p["q"])
+    l = torch.empty((64, 32), dtype=torch.float32, device=dev)
+    ws = torch.empty(attn.attn_paged_decode_workspace_size(64, 32, 128, 64, 128), dtype=torch.uint8, device=dev)
+
+    def dec():
+        attn.paged_decode(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], out=o, lse=l,
+                          workspace=ws)
+    dec()
+    ms = timed_launches(torch, dec, reps, flush)
+    attn.device_status()
+    total_tokens = int(p["seq_lens"].sum().item())
+    n_pages = int(((p["seq_lens"].long() + 63) // 64).sum().item())
+    alg_bytes = total_tokens * 32 * 128 * 2 * 2 + 2 * (64 * 32 * 128 * 2) + 64 * 32 * 4 + n_pages * 4 + 64 * 4
+    gbs = alg_bytes / (statistics.mean(ms) * 1e-3) / 1e9
+    out["paged_decode_64req_H32_d128_p64"] = {
+        "GBps": round(gbs, 1), "ms": round(statistics.mean(ms), 4), "algorithmic_bytes": alg_bytes,
+        "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4), "frac_of_8TBps": round(gbs / 8000.0, 4),
+        "tokens": total_tokens}
+    del p, o, l, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle (reference arm and cpu_baseline)
+
+class OracleSampler:
+    """Times the float64 oracle on row samples of the step's workload (inputs
+    generated once; the per-row cost calibrated once)."""
+
+    def __init__(self):
+        import numpy as np
+
+        import oracle
+        from attention_attn_fwd_03_gb300 import inputs
+
+        self.np, self.oracle = np, oracle
+        self.q, self.k, self.v = inputs.dense_qkv(B, H, N, N, D, seed=0)
+        self.scale = float(np.float32(1.0 / math.sqrt(D)))
+        self.threads = oracle.default_threads()
+        self.rng = np.random.default_rng(0)
+        cal = np.sort(self.rng.choice(B * H * N, size=256, replace=False))
+        t0 = time.perf_counter()
+        oracle.attention(self.q, self.k, self.v, self.scale, causal=False, rows=cal, nthreads=self.threads)
+        self.per_row = max((time.perf_counter() - t0) / 256, 1e-7)
+
+    def run(self, seconds):
+        """One timed sample of about `seconds` of CPU work: the same rows, non-causal
+        then causal.  Returns (TFLOPS-equivalent, seconds, description)."""
+        np = self.np
+        n = int(min(B * H * N, max(256, seconds / 1.5 / self.per_row)))
+        rows = np.sort(self.rng.choice(B * H * N, size=n, replace=False))
+        t0 = time.perf_counter()
+        self.oracle.attention(self.q, self.k, self.v, self.scale, causal=False, rows=rows, nthreads=self.threads)
+        self.oracle.attention(self.q, self.k, self.v, self.scale, causal=True, rows=rows, nthreads=self.threads)
+        secs = time.perf_counter() - t0
+        flops = 4.0 * D * N * n + 4.0 * D * float(np.sum(rows % N + 1))
+        desc = ("float64 oracle (three-pass softmax per row) on %d of %d rows, non-causal and causal, "
+                "of the step's workload; FLOPs = 4*d per visible (row, key) pair" % (n, B * H * N))
+        return flops / secs / 1e12, secs, desc
+
+
+def cpu_baseline(sample_seconds):
+    sampler = OracleSampler()
+    val, secs, desc = sampler.run(sample_seconds)
+    return {"value": round(val, 6), "unit": "TFLOPS", "cores": sampler.threads, "kind": "oracle",
+            "sample": desc, "seconds": round(secs, 2)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    sampler = OracleSampler()
+    per_step = max(0.2, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        sampler.run(per_step / 2)
+    vals, secs, desc = [], [], ""
+    for _ in range(args.steps):
+        v, s, desc = sampler.run(per_step)
+        vals.append(v)
+        secs.append(s)
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.mean(secs), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), rounded to bf16)",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": sampler.threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,131 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * Three operations, all computing exact scaled-dot-product attention
+ *     O = softmax(scale * Q K^T) V
+ * ("FlashAttention V3 实战: Hopper 架构下的 Paged KV Cache 协同优化",
+ * section 一, the attention formula; "Capstone: CUDA Softmax 与 Attention
+ * 算子", section 1.1) in one tiled pass with the online-softmax running max m
+ * and denominator l (same Capstone page, section 2.2 steps 3-5, and section
+ * 4.1-4.2 for the loop order and the single final division), so the score
+ * and probability matrices never reach device memory.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing and frees nothing; it keeps only per-device
+ *     cached kernel attributes and one device status word (see
+ *     attn_device_status).
+ *   - Layouts are dense row-major ("BHSD"): element (b, h, i, c) of a
+ *     [B, H, N, d] tensor is at ((b*H + h)*N + i)*d + c.
+ *   - Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous: they validate their arguments on the
+ *     host, enqueue kernels and return; nothing synchronises.
+ *   - A non-ATTN_OK return from argument validation means nothing was
+ *     enqueued and no output was touched.
+ *   - LSE is the natural-log log-sum-exp of the scaled scores of the row's
+ *     valid keys: lse = m + ln(l).  A row with no valid key has O = 0 and
+ *     lse = -inf.
+ *   - Causal masking is the lower-triangular mask aligned to the bottom
+ *     right: key j is visible to query i iff j <= i + (Nk - Nq) (the pages'
+ *     "下三角" mask, Capstone page section 7.3; identical to j <= i when
+ *     Nq == Nk).
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* NULL pointer, non-positive size, misalignment, bad scale */
+    ATTN_ERR_UNSUPPORTED = 2,  /* a head dim / page size / dtype this build has no kernel for */
+    ATTN_ERR_CUDA = 3,         /* a CUDA runtime call or a kernel launch failed */
+    ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than the size query asked for */
+    ATTN_ERR_TIMEOUT = 5,      /* a kernel's bounded wait gave up (device status word) */
+    ATTN_ERR_DEVICE_DATA = 6   /* a device-side length or page id was out of range (status word) */
+} attn_status_t;
+
+/* Dense prefill, bf16.
+ *   q: bf16 [B, H, Nq, d]; k, v: bf16 [B, H, Nk, d]   (read only)
+ *   o: bf16 [B, H, Nq, d]                               (written)
+ *   lse: fp32 [B, H, Nq] or NULL                        (written when non-NULL)
+ *   d in {64, 128}; B, H, Nq, Nk >= 1; B*H < 2^31; scale finite and > 0
+ *   (1/sqrt(d) for standard attention); causal 0 or 1.
+ * Output rounding: O is rounded once from fp32 to bf16 (nearest-even).
+ * Errors: ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED before any launch;
+ * ATTN_ERR_CUDA when the launch fails. */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                       void* stream);
+
+/* Dense prefill on FP8-e4m3fn inputs ("Flash Attention 3 指南", the FP8
+ * path: e4m3 operands, fp32-accumulated products, P cast to e4m3 before the
+ * P*V product, 16-bit output).
+ *   q8, k8, v8: e4m3fn codes, [B, H, Nq|Nk, d] like attn_fwd;
+ *   q_descale, k_descale, v_descale: per-tensor factors, the real value of a
+ *   code x is decode(x) * descale (with per-tensor amax scaling the descale
+ *   is amax / 448);
+ *   o: bf16 [B, H, Nq, d]; lse: fp32 [B, H, Nq] or NULL.
+ *   Scores are scale * q_descale * k_descale * (q8 . k8); the unnormalised
+ *   probabilities are rounded to e4m3 (nearest, saturating) before the P*V
+ *   product while l sums them in fp32; O = v_descale * (P8 V8) / l.
+ *   d must be 128.  Errors as attn_fwd. */
+attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
+                           float q_descale, float k_descale, float v_descale,
+                           void* o, float* lse,
+                           int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                           void* stream);
+
+/* Bytes of device workspace attn_paged_decode needs for these sizes
+ * (0 on invalid sizes).  The workspace holds the per-split partial results
+ * (unnormalised O, m, l) that the merge step combines. */
+size_t attn_paged_decode_workspace_size(int B, int H, int d, int page_size, int max_pages_per_seq);
+
+/* One-token decode over a paged KV cache ("FlashAttention V3 实战", section
+ * 3.2: vLLM/SGLang-style page tables).  Each request's keys are split into
+ * chunks of pages that are processed independently; the partial results are
+ * combined with the (m, l, O) merge of the Capstone page, section 2.2 step 4:
+ *   m = max_s m_s,  l = sum_s l_s e^(m_s - m),  O = sum_s e^(m_s - m) O_s / l.
+ *   q: bf16 [B, H, d] (one query token per request)
+ *   k_cache, v_cache: bf16 [num_pages, page_size, H, d]
+ *   block_table: int32 [B, max_pages_per_seq], physical page ids
+ *   seq_lens: int32 [B], keys 0..seq_lens[r]-1 of request r are attended;
+ *     key t lives at cache[block_table[r][t / page_size]][t % page_size]
+ *   o: bf16 [B, H, d]; lse: fp32 [B, H] or NULL
+ *   workspace: device buffer of at least
+ *     attn_paged_decode_workspace_size(B, H, d, page_size, max_pages_per_seq)
+ *     bytes, owned by the caller, contents need no initialisation.
+ *   d in {64, 128}; page_size a multiple of 8 in [8, 1024].
+ * Device-side data (seq_lens, block_table) is the caller's contract: a
+ * length outside [0, max_pages_per_seq*page_size] is clamped and a page id
+ * outside [0, num_pages) is skipped; either sets the device status word to
+ * ATTN_ERR_DEVICE_DATA (read it with attn_device_status). */
+attn_status_t attn_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens,
+                                int B, int H, int d, int page_size, int max_pages_per_seq,
+                                int num_pages, float scale, void* o, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then reads and clears the calling device's status
+ * word.  Kernels set it when a bounded internal wait gives up
+ * (ATTN_ERR_TIMEOUT; the kernel then returns early and its outputs are
+ * undefined) or when paged-decode device data is out of range
+ * (ATTN_ERR_DEVICE_DATA).  While the word is set, prefill kernels return
+ * without work, so check it after any call whose result matters.
+ * Returns ATTN_OK, one of those two codes, or ATTN_ERR_CUDA. */
+attn_status_t attn_device_status(void* stream);
+
+/* Static English description of a status code (never NULL). */
+const char* attn_status_string(attn_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

@@ -1,0 +1,117 @@
+"""The C-ABI library: builds for sm_103a, loads without a GPU, exports every
+entry point include/attn.h declares, and rejects bad arguments on the host
+before touching the device.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_attn_fwd_03_gb300 as attn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    attn.build()
+    return attn.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    assert _declared() == sorted(["attn_fwd", "attn_fwd_fp8", "attn_paged_decode",
+                                  "attn_paged_decode_workspace_size", "attn_device_status",
+                                  "attn_status_string"])
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared():
+        assert hasattr(L, name), name
+    raw = ctypes.CDLL(attn.LIB_PATH)
+    for name in _declared():
+        assert ctypes.cast(getattr(raw, name), ctypes.c_void_p).value
+
+
+def test_status_strings(L):
+    for code in range(7):
+        s = attn.attn_status_string(code)
+        assert s and s != "unknown status"
+    assert attn.attn_status_string(99) == "unknown status"
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-NULL address; validation fails before any use
+
+
+def _fwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, H=1, Nq=128, Nk=128, d=128, scale=0.088,
+             causal=0, stream=None)
+    a.update(kw)
+    return attn.attn_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=None), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Nq=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), attn.ATTN_ERR_INVALID_ARG),
+    (dict(lse=FAKE + 2), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+])
+def test_fwd_validation(L, kw, code):
+    assert _fwd(**kw) == code
+
+
+def test_fp8_validation(L):
+    base = dict(q8=FAKE, k8=FAKE, v8=FAKE, q_descale=1.0, k_descale=1.0, v_descale=1.0, o=FAKE, lse=None,
+                B=1, H=1, Nq=64, Nk=64, d=128, scale=0.088, causal=0, stream=None)
+    assert attn.attn_fwd_fp8(**dict(base, q_descale=0.0)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_fp8(**dict(base, v_descale=float("inf"))) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_fp8(**dict(base, d=64)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_fwd_fp8(**dict(base, k8=None)) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_workspace_size_query(L):
+    ws = attn.attn_paged_decode_workspace_size(64, 32, 128, 64, 128)
+    assert ws >= 64 * 32 * 130 * 4  # at least one (O, m, l) record per (request, head)
+    assert attn.attn_paged_decode_workspace_size(64, 32, 128, 64, 256) > ws
+    assert attn.attn_paged_decode_workspace_size(64, 32, 96, 64, 128) == 0
+    assert attn.attn_paged_decode_workspace_size(64, 32, 128, 12, 128) == 0
+    assert attn.attn_paged_decode_workspace_size(0, 32, 128, 64, 128) == 0
+
+
+def test_paged_decode_validation(L):
+    ws = attn.attn_paged_decode_workspace_size(4, 2, 128, 64, 8)
+    base = dict(q=FAKE, k_cache=FAKE, v_cache=FAKE, block_table=FAKE, seq_lens=FAKE, B=4, H=2, d=128,
+                page_size=64, max_pages_per_seq=8, num_pages=32, scale=0.088, o=FAKE, lse=None,
+                workspace=FAKE, workspace_bytes=ws, stream=None)
+    assert attn.attn_paged_decode(**dict(base, workspace_bytes=ws - 1)) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_paged_decode(**dict(base, workspace=None)) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_paged_decode(**dict(base, page_size=12)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_paged_decode(**dict(base, d=80)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_paged_decode(**dict(base, seq_lens=None)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_paged_decode(**dict(base, block_table=FAKE + 2)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_paged_decode(**dict(base, num_pages=0)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_paged_decode(**dict(base, scale=-1.0)) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_library_has_no_oracle_dependency():
+    """The product library links nothing from oracle/, and its sources name none of it."""
+    csrc = os.path.join(ROOT, "attention_attn_fwd_03_gb300", "csrc")
+    for f in os.listdir(csrc):
+        text = open(os.path.join(csrc, f), encoding="utf-8").read()
+        assert "oracle" not in text.lower(), f
+    for f in ("__init__.py", "_build.py", "inputs.py"):
+        text = open(os.path.join(ROOT, "attention_attn_fwd_03_gb300", f), encoding="utf-8").read()
+        assert "import oracle" not in text and "from oracle" not in text, f
