@@ -107,6 +107,21 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// AND of `pred` over the `nthreads` threads of named barrier `id` (all of them
+// must arrive); gives every thread of a warpgroup the same decision.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pin, pout;\n\t"
+        "setp.ne.u32 pin, %1, 0;\n\t"
+        "bar.red.and.pred pout, %2, %3, pin;\n\t"
+        "selp.u32 %0, 1, 0, pout;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -258,10 +273,9 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int it = 0; it < n_t; ++it) {
-        if (!wait_bar(&b.s_full[t], (uint32_t)(it & 1), abort_flag, p.status)) {
-            ok = false;
-            break;
-        }
+        // every lane of the warp takes the same branch (tcgen05.ld is warp-collective)
+        ok = __all_sync(0xffffffffu, wait_bar(&b.s_full[t], (uint32_t)(it & 1), abort_flag, p.status));
+        if (!ok) break;
         tc_fence_after();
         uint32_t s[128];
         tmem_ld32(tS + 0, s);
@@ -343,9 +357,11 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
 
     // ---- epilogue: O / l -> bf16 -> shared (128B-swizzled) -> TMA store; LSE
     if (ok && n_t > 0) {
-        if (!wait_bar(&b.o_full[t], 0, abort_flag, p.status)) ok = false;
+        ok = __all_sync(0xffffffffu, wait_bar(&b.o_full[t], 0, abort_flag, p.status));
         tc_fence_after();
     }
+    // one decision for the whole warpgroup before its named barriers
+    ok = named_bar_and(1 + t, 128, ok);
     if (!ok) return;
     const float m_use = (m == -INFINITY) ? 0.f : m;
     const float inv = (l > 0.f) ? p.o_scale / l : 0.f;

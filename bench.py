@@ -67,56 +67,110 @@ def dist_env():
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons during the timed region."""
+    """Samples the SM clock and the clock-event (throttle) reasons DURING the
+    timed region: NVML through ctypes every ~2 ms from a background thread
+    (reading only), plus an nvidia-smi process at 200 ms as a second source."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
-        self.proc = None
+    def __init__(self, torch, device_index):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self.smi_lines = []
+        self._stop = False
+        self._nvml = None
+        self._handle = None
+        self._proc = None
+        self._smi_index = str(device_index)
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() == 0:
+                h = ctypes.c_void_p()
+                bus = None
+                try:
+                    pr = torch.cuda.get_device_properties(device_index)
+                    bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+                except Exception:
+                    bus = None
+                ok = bus is not None and nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+                if not ok:
+                    ok = nv.nvmlDeviceGetHandleByIndex_v2(int(device_index), ctypes.byref(h)) == 0
+                if ok:
+                    self._nvml, self._handle, self._ct = nv, h, ctypes
+                    idx = ctypes.c_uint()
+                    if nv.nvmlDeviceGetIndex(h, ctypes.byref(idx)) == 0:
+                        self._smi_index = str(idx.value)
+                    mx = ctypes.c_uint()
+                    if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                        self.max_mhz = float(mx.value)
+        except Exception:
+            self._nvml = None
+
+    def _poll(self):
+        ct, nv, h = self._ct, self._nvml, self._handle
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop:
+            if nv.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0:
+                self.samples.append(float(clk.value))
+            if get_reasons(h, ct.byref(rs)) == 0:
+                for name, bit in self.REASON_BITS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.002)
 
     def __enter__(self):
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self._smi_index, "--query-gpu=" + self.SMI_FIELDS,
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
-            self.proc = None
+            self._proc = None
+        self._thread = None
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *a):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop = True
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                out, _ = self._proc.communicate(timeout=5)
             except Exception:
-                self.proc.kill()
+                self._proc.kill()
                 out = ""
-            self.lines = [ln for ln in (out or "").splitlines() if ln.strip()]
+            self.smi_lines = [ln for ln in (out or "").splitlines() if ln.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
+        smi_sm, reasons = [], set(self.reasons)
+        mx = self.max_mhz
+        for ln in self.smi_lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                smi_sm.append(float(parts[0]))
+                mx = max(mx or 0.0, float(parts[1]))
             except ValueError:
                 continue
             for nm, val in zip(names, parts[4:8]):
                 if val.lower() == "active":
                     reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        sm = self.samples or smi_sm
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "source": "nvml" if self.samples else ("nvidia-smi" if smi_sm else "none")}
 
 
 # ---------------------------------------------------------------- timing helpers
@@ -199,7 +253,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
+    with ClockSampler(torch, local_rank) as clk:
         for i in range(args.steps):
             flush()
             starts[i].record(stream)
@@ -427,19 +481,67 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """Small fixed workloads for ncu captures: warm-up, then --steps launches of one case."""
+    import torch
+
+    import attention_attn_fwd_03_gb300 as attn
+    from attention_attn_fwd_03_gb300 import inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    attn.lib()
+    case = args.profile_case
+    if case == "step":
+        q, k, v = (t.to(dev) for t in inputs.dense_qkv(B, H, N, N, D, seed=0))
+        fns = [lambda: attn.fwd(q, k, v, causal=False), lambda: attn.fwd(q, k, v, causal=True)]
+    elif case == "long_small":
+        q, k, v = (t.to(dev) for t in inputs.dense_qkv(1, 4, 32768, 32768, 128, seed=0))
+        fns = [lambda: attn.fwd(q, k, v, causal=True)]
+    elif case == "fp8":
+        q, k, v = inputs.dense_qkv(2, 16, 8192, 8192, 128, seed=0)
+        (q8, dq), (k8, dk), (v8, dv) = (inputs.fp8_quantize(t) for t in (q, k, v))
+        q8, k8, v8 = q8.to(dev), k8.to(dev), v8.to(dev)
+        fns = [lambda: attn.fwd_fp8(q8, k8, v8, (dq, dk, dv))]
+    elif case == "decode_small":
+        p = inputs.paged_kv(B=8, H=32, d=128, page_size=64, max_pages=128, num_pages=1024, len_lo=512,
+                            len_hi=8192, seed=0, device=dev)
+        fns = [lambda: attn.paged_decode(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"])]
+    else:
+        raise SystemExit("unknown --profile-case %s" % case)
+    for _ in range(args.warmup):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        for f in fns:
+            f()
+    e.record()
+    e.synchronize()
+    attn.device_status()
+    print(json.dumps({"profile_case": case, "launches": args.steps * len(fns),
+                      "ms_per_iteration": s.elapsed_time(e) / args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", choices=["step", "long_small", "fp8", "decode_small"], default=None,
+                    help="run one small workload for an ncu capture instead of the benchmark")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     rank, world, local_rank = dist_env()
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)
