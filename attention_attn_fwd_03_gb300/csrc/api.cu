@@ -28,6 +28,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     bool ready = false;
     unsigned* status = nullptr;
+    int sm_count = 0;
 };
 
 std::mutex g_mu;
@@ -46,6 +47,9 @@ attn_status_t device_state(DeviceState** out) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return ATTN_ERR_CUDA;
         s.status = static_cast<unsigned*>(ptr);
+        if (cudaDeviceGetAttribute(&s.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            s.sm_count < 1)
+            return ATTN_ERR_CUDA;
         s.ready = true;
     }
     if (!g_encode) {
@@ -63,18 +67,19 @@ attn_status_t device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 3-D map over a [BH, rows, d] tensor: box = (128 bytes of d, 128 rows, 1),
-// 128-byte swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* map, const void* base, bool fp8, int d, long long rows, long long bh) {
+// 3-D map over a [BH, rows, d] tensor.  Operand maps: box = (128 bytes of d,
+// 128 rows, 1) with 128-byte swizzle; output map: box = (32 elements, 32
+// rows, 1), no swizzle.  Zero fill outside the tensor; stores are clipped.
+bool make_map(CUtensorMap* map, const void* base, bool fp8, int d, long long rows, long long bh, bool out) {
     const int eb = fp8 ? 1 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
     cuuint64_t strides[2] = {(cuuint64_t)d * eb, (cuuint64_t)rows * d * eb};
-    cuuint32_t box[3] = {(cuuint32_t)(128 / eb), 128u, 1u};
+    cuuint32_t box[3] = {out ? 32u : (cuuint32_t)(128 / eb), out ? 32u : 128u, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          out ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -99,8 +104,8 @@ attn_status_t prefill(const void* q, const void* k, const void* v, void* o, floa
     const long long BH = (long long)B * H;
     PrefillParams p;
     std::memset(&p, 0, sizeof p);
-    if (!make_map(&p.tm_q, q, fp8, d, Nq, BH) || !make_map(&p.tm_k, k, fp8, d, Nk, BH) ||
-        !make_map(&p.tm_v, v, fp8, d, Nk, BH) || !make_map(&p.tm_o, o, false, d, Nq, BH))
+    if (!make_map(&p.tm_q, q, fp8, d, Nq, BH, false) || !make_map(&p.tm_k, k, fp8, d, Nk, BH, false) ||
+        !make_map(&p.tm_v, v, fp8, d, Nk, BH, false) || !make_map(&p.tm_o, o, false, d, Nq, BH, true))
         return ATTN_ERR_CUDA;
     p.lse = lse;
     p.status = ds->status;
@@ -112,9 +117,11 @@ attn_status_t prefill(const void* q, const void* k, const void* v, void* o, floa
     const float log2e = 1.4426950408889634f;
     p.c_scale = fp8 ? scale * dq * dk * log2e : scale * log2e;
     p.o_scale = fp8 ? dv : 1.f;
-    const long long grid = (long long)p.n_pairs * BH;
-    if (grid > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
-    return from_cuda(launch_prefill(d, fp8, p, (int)grid, static_cast<cudaStream_t>(stream)));
+    const long long units = (long long)p.n_pairs * BH;
+    if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    p.n_units = (int)units;
+    const int grid = units < ds->sm_count ? (int)units : ds->sm_count;  // persistent: one CTA per SM
+    return from_cuda(launch_prefill(d, fp8, p, grid, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace

@@ -8,8 +8,9 @@
 
 namespace attn {
 
-// Dense prefill.  Q/K/V/O are described by 3-D TMA maps over
-// (d, rows, B*H) with a 128-row box, 128-byte swizzle and zero fill.
+// Dense prefill.  Q/K/V are described by 3-D TMA maps over (d, rows, B*H)
+// with a (128 bytes, 128 rows) box, 128-byte swizzle and zero fill; O by a
+// map with a (32 elements, 32 rows) box and no swizzle (per-warp stores).
 struct PrefillParams {
     CUtensorMap tm_q;
     CUtensorMap tm_k;
@@ -18,14 +19,16 @@ struct PrefillParams {
     float* lse;         // [B*H, Nq] or nullptr
     unsigned* status;   // device status word (bit mask of ATTN_ERR_* codes)
     int BH, Nq, Nk, causal;
-    int n_pairs;        // ceil(Nq / 256): each CTA owns two 128-row query tiles
+    int n_pairs;        // ceil(Nq / 256): a work unit is two 128-row query tiles
+    int n_units;        // n_pairs * B * H
     float c_scale;      // scale * log2(e) [* q_descale * k_descale]
     float o_scale;      // 1 [or v_descale]
 };
 
-constexpr int kPrefillThreads = 320;  // 2 softmax warpgroups + MMA warp + TMA warp
+constexpr int kPrefillThreads = 352;  // 2 MMA issuer warps + TMA warp + 2 softmax warpgroups
 
 int prefill_smem_bytes(int d, bool fp8);
+// grid = number of persistent CTAs (at most one per SM and at most n_units)
 cudaError_t launch_prefill(int d, bool fp8, const PrefillParams& p, int grid, cudaStream_t stream);
 
 // Paged decode: split kernel writes per-split partials, merge kernel combines.
