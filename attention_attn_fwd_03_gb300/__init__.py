@@ -69,6 +69,8 @@ def lib():
             L.attn_paged_decode_workspace_size.argtypes = [i, i, i, i, i]
             L.attn_paged_decode.restype = i
             L.attn_paged_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
+            L.attn_paged_decode_noalloc.restype = i
+            L.attn_paged_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp]
             L.attn_device_status.restype = i
             L.attn_device_status.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -97,6 +99,14 @@ def attn_paged_decode(q, k_cache, v_cache, block_table, seq_lens, B, H, d, page_
     return lib().attn_paged_decode(q, k_cache, v_cache, block_table, seq_lens, B, H, d, page_size,
                                    max_pages_per_seq, num_pages, scale, o, lse, workspace, workspace_bytes,
                                    stream)
+
+
+def attn_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, B, H, d, page_size,
+                              max_pages_per_seq, num_pages, scale, o, lse, stream):
+    """Paged decode whose split partials live in the library's fixed device
+    scratch array; allocates nothing (see include/attn.h for its limits)."""
+    return lib().attn_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, B, H, d, page_size,
+                                           max_pages_per_seq, num_pages, scale, o, lse, stream)
 
 
 def attn_device_status(stream):

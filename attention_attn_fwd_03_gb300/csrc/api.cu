@@ -125,6 +125,16 @@ attn_status_t prefill(const void* q, const void* k, const void* v, void* o, floa
 }
 
 }  // namespace
+
+// Device address of the calling device's status word (set-up on first use).
+attn_status_t status_word_address(unsigned** out) {
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    *out = ds->status;
+    return ATTN_OK;
+}
+
 }  // namespace attn
 
 using namespace attn;

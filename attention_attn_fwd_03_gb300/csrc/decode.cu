@@ -21,6 +21,9 @@
 // Merge kernel: one warp per (request, head) combines the splits with the
 // (m, l, O) merge of section 2.2 step 4:
 //   m = max_s m_s,  l = sum_s l_s 2^(m_s - m),  O = sum_s 2^(m_s - m) O_s / l.
+#include <cmath>
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -251,3 +254,119 @@ cudaError_t launch_paged_decode(int d, const DecodeParams& p, cudaStream_t strea
 }
 
 }  // namespace attn
+
+// ---------------------------------------------------------------- allocation-free variant
+//
+// attn_paged_decode_noalloc: the same split + merge kernels, with the
+// split partials kept in a fixed device array of ATTN_NOALLOC_SCRATCH_BYTES
+// that this file owns instead of a caller-provided workspace.  The array is
+// part of the library image: every device that loads the library holds it
+// until the process exits.  In host code its name is only a host-side
+// stand-in, so its device address is looked up once per device with
+// cudaGetSymbolAddress and passed to the kernels.
+
+namespace attn {
+
+static __device__ __align__(256) unsigned char g_decode_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxScratchDevices];
+
+// Device address of the scratch array on the current device (first call per
+// device resolves it; that first call should happen before any stream capture).
+cudaError_t scratch_address(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = ptr;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+// Split plan for the fixed scratch: the default number of pages per split,
+// coarsened until the partials fit in `cap` bytes.  Returns false when even
+// one split per request does not fit.
+bool capped_plan(int B, int H, int d, int page_size, int max_pages, size_t cap, DecodePlan* out) {
+    int pps = 128 / page_size;
+    if (pps < 1) pps = 1;
+    for (;;) {
+        DecodePlan pl{};
+        pl.pages_per_split = pps;
+        pl.max_splits = (max_pages + pps - 1) / pps;
+        const size_t recs = (size_t)B * H * pl.max_splits;
+        pl.part_o_bytes = recs * d * sizeof(float);
+        pl.part_ml_bytes = recs * 2 * sizeof(float);
+        pl.workspace_bytes = (pl.part_o_bytes + 255) / 256 * 256 + pl.part_ml_bytes;
+        if (pl.workspace_bytes <= cap) {
+            *out = pl;
+            return true;
+        }
+        if (pps >= max_pages) return false;
+        ++pps;
+    }
+}
+
+}  // namespace
+
+}  // namespace attn
+
+extern "C" attn_status_t attn_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                                   const int32_t* block_table, const int32_t* seq_lens, int B,
+                                                   int H, int d, int page_size, int max_pages_per_seq,
+                                                   int num_pages, float scale, void* o, float* lse,
+                                                   void* stream) {
+    using namespace attn;
+    auto a16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || max_pages_per_seq < 1 || num_pages < 1 || page_size < 1) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (!a16(q) || !a16(k_cache) || !a16(v_cache) || !a16(o)) return ATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return ATTN_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_ERR_INVALID_ARG;
+    if ((d != 64 && d != 128) || page_size < 8 || page_size > 1024 || page_size % 8 != 0)
+        return ATTN_ERR_UNSUPPORTED;
+    if ((long long)max_pages_per_seq * page_size > 0x7fffffffLL || (long long)B * max_pages_per_seq > 0x7fffffffLL)
+        return ATTN_ERR_INVALID_ARG;
+    DecodePlan pl{};
+    if (!capped_plan(B, H, d, page_size, max_pages_per_seq, (size_t)ATTN_NOALLOC_SCRATCH_BYTES, &pl))
+        return ATTN_ERR_WORKSPACE;  // the partials of even one split per request exceed the fixed scratch
+    if (pl.max_splits > 65535 || B > 65535) return ATTN_ERR_UNSUPPORTED;
+
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned* status = nullptr;
+    attn_status_t st = status_word_address(&status);
+    if (st != ATTN_OK) return st;
+
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.k_cache = static_cast<const uint16_t*>(k_cache);
+    p.v_cache = static_cast<const uint16_t*>(v_cache);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.part_o = static_cast<float*>(scratch);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) + (pl.workspace_bytes - pl.part_ml_bytes));
+    p.o = static_cast<uint16_t*>(o);
+    p.lse = lse;
+    p.status = status;
+    p.B = B;
+    p.H = H;
+    p.page_size = page_size;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.pages_per_split = pl.pages_per_split;
+    p.max_splits = pl.max_splits;
+    p.c_scale = scale * 1.4426950408889634f;
+    return launch_paged_decode(d, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}

@@ -61,3 +61,12 @@ DecodePlan decode_plan(int B, int H, int d, int page_size, int max_pages);
 cudaError_t launch_paged_decode(int d, const DecodeParams& p, cudaStream_t stream);
 
 }  // namespace attn
+
+#include "attn.h"
+
+namespace attn {
+
+// Device address of the calling device's status word (api.cu).
+attn_status_t status_word_address(unsigned** out);
+
+}  // namespace attn

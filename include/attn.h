@@ -112,6 +112,35 @@ attn_status_t attn_paged_decode(const void* q, const void* k_cache, const void* 
                                 int num_pages, float scale, void* o, float* lse,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the fixed device scratch array used by attn_paged_decode_noalloc. */
+#define ATTN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* Paged decode without any allocation (no counterpart on the attention pages:
+ * an addition for callers).  Some callers cannot allocate device memory at
+ * call time: a serving loop whose device memory is fully reserved up front
+ * for its own KV-cache pool, or one that forbids cudaMalloc after start-up
+ * because it can synchronise the device and stall other streams.  This entry
+ * point takes the same arguments as attn_paged_decode minus the workspace and
+ * computes the same result; the split partials live in a fixed device array
+ * of ATTN_NOALLOC_SCRATCH_BYTES owned by the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   - The first call on a device looks up that array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (on
+ *     different streams, or from different host threads without ordering)
+ *     race and give undefined results.  Partials from an earlier call are
+ *     never read, so nothing needs clearing between calls.
+ *   - If the partials do not fit, the split is coarsened (more pages per
+ *     split); if even one split per request exceeds the array, the call
+ *     returns ATTN_ERR_WORKSPACE and enqueues nothing.
+ *   - Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating
+ *     library routine is called.
+ * Other errors and the device-data contract are as for attn_paged_decode. */
+attn_status_t attn_paged_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, const int32_t* seq_lens,
+                                        int B, int H, int d, int page_size, int max_pages_per_seq,
+                                        int num_pages, float scale, void* o, float* lse, void* stream);
+
 /* Synchronises `stream`, then reads and clears the calling device's status
  * word.  Kernels set it when a bounded internal wait gives up
  * (ATTN_ERR_TIMEOUT; the kernel then returns early and its outputs are

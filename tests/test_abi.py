@@ -26,8 +26,8 @@ def _declared():
 
 def test_header_declares_the_entry_points():
     assert _declared() == sorted(["attn_fwd", "attn_fwd_fp8", "attn_paged_decode",
-                                  "attn_paged_decode_workspace_size", "attn_device_status",
-                                  "attn_status_string"])
+                                  "attn_paged_decode_workspace_size", "attn_paged_decode_noalloc",
+                                  "attn_device_status", "attn_status_string"])
 
 
 def test_every_declared_symbol_is_exported(L):
