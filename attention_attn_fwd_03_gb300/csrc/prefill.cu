@@ -238,30 +238,27 @@ __device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars&
 template <int D, bool FP8>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t a0, uint64_t b0) {
     using C = Cfg<D, FP8>;
+    // four 32-byte K steps per 128-byte panel; next panel PANEL_BYTES further
 #pragma unroll
-    for (int k = 0; k < C::S_STEPS; ++k) {
-        const uint64_t off = (uint64_t)(((k >> 2) * C::PANEL_BYTES + (k & 3) * 32) >> 4);
-        if (FP8)
-            mma_f8_ss(d_tmem, a0 + off, b0 + off, C::ID_S, k > 0 ? 1u : 0u);
-        else
-            mma_f16_ss(d_tmem, a0 + off, b0 + off, C::ID_S, k > 0 ? 1u : 0u);
+    for (int g = 0; g < C::S_STEPS / 4; ++g) {
+        const uint64_t po = (uint64_t)((g * C::PANEL_BYTES) >> 4);
+        mma4_ss<2, 4, 6, 2, 4, 6, FP8>(d_tmem, a0 + po, b0 + po, C::ID_S, g > 0 ? 1u : 0u);
     }
 }
 
-// O += P V: PV_STEPS MMAs along the keys; P from tensor memory, b0 the
-// descriptor of the MN-major V tile (step s starts s * MMA_K rows further).
+// O += P V: PV_STEPS MMAs along the keys; P from tensor memory (P_STEP_COLS
+// columns per step), b0 the descriptor of the MN-major V tile (step s starts
+// s * MMA_K rows, i.e. s * MMA_K * 128 bytes, further).
 template <int D, bool FP8>
 __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t b0, bool accumulate) {
     using C = Cfg<D, FP8>;
+    constexpr int PC = (int)C::P_STEP_COLS;
+    constexpr int VB = (C::MMA_K * 128) >> 4;
 #pragma unroll
-    for (int s = 0; s < C::PV_STEPS; ++s) {
-        const uint64_t bd = b0 + (uint64_t)((s * C::MMA_K * 128) >> 4);
-        const uint32_t acc = (accumulate || s > 0) ? 1u : 0u;
-        if (FP8)
-            mma_f8_ts(o_tmem, p_tmem + s * C::P_STEP_COLS, bd, C::ID_PV, acc);
-        else
-            mma_f16_ts(o_tmem, p_tmem + s * C::P_STEP_COLS, bd, C::ID_PV, acc);
-    }
+    for (int g = 0; g < C::PV_STEPS / 4; ++g)
+        mma4_ts<PC, 2 * PC, 3 * PC, VB, 2 * VB, 3 * VB, FP8>(o_tmem, p_tmem + (uint32_t)(4 * g * PC),
+                                                           b0 + (uint64_t)(4 * g * VB), C::ID_PV,
+                                                           (accumulate || g > 0) ? 1u : 0u);
 }
 
 // MMA issuers: warp t issues query tile t's GEMMs.  The two issuers take
@@ -423,17 +420,17 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
                     if (key >= p.Nk || (p.causal && (long long)key > limit)) s[c] = __float_as_uint(-INFINITY);
                 }
             }
-            // row max: four independent chains of 3-input max
-            float mc[4];
+            // row max: eight independent chains of 3-input max
+            float mc[8];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float x = __uint_as_float(s[32 * q]);
+            for (int q = 0; q < 8; ++q) {
+                float x = __uint_as_float(s[16 * q]);
 #pragma unroll
-                for (int i = 1; i < 31; i += 2)
-                    x = max3(x, __uint_as_float(s[32 * q + i]), __uint_as_float(s[32 * q + i + 1]));
-                mc[q] = fmaxf(x, __uint_as_float(s[32 * q + 31]));
+                for (int i = 1; i < 15; i += 2)
+                    x = max3(x, __uint_as_float(s[16 * q + i]), __uint_as_float(s[16 * q + i + 1]));
+                mc[q] = fmaxf(x, __uint_as_float(s[16 * q + 15]));
             }
-            const float mx = fmaxf(max3(mc[0], mc[1], mc[2]), mc[3]);
+            const float mx = fmaxf(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], max3(mc[5], mc[6], mc[7])));
             const float m_cand = mx * cs;
             float alpha = 1.f;
             bool resc = false;

@@ -59,6 +59,21 @@ __device__ __forceinline__ bool bar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As bar_try_wait, but the thread may sleep in hardware for up to
+// `suspend_ns` while the phase is incomplete instead of returning at once,
+// so waiting warps do not take issue slots from working ones.
+__device__ __forceinline__ bool bar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (after flagging the CTA and the device status word) on timeout, or
 // when another role of the CTA, or another CTA, has already given up.
@@ -67,7 +82,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     if (bar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-        if (bar_try_wait(bar, parity)) return true;
+        if (bar_try_wait_sleep(bar, parity, 20000u)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
             if (*(volatile unsigned*)status != 0u) {
@@ -178,6 +193,66 @@ __device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// Four tcgen05.mma of one GEMM in a single asm block (one predicate set-up,
+// no address arithmetic between them): step k uses descriptors a + OA_k and
+// b + OB_k (descriptor units: 16 bytes), or for a tensor-memory A operand the
+// column a + OA_k; the first step accumulates iff `accumulate`.
+template <int OA1, int OA2, int OA3, int OB1, int OB2, int OB3, bool F8>
+__device__ __forceinline__ void mma4_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    if (F8)
+        asm volatile(
+            "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+            "add.s64 a1, %1, %5;\n\tadd.s64 a2, %1, %6;\n\tadd.s64 a3, %1, %7;\n\t"
+            "add.s64 b1, %2, %8;\n\tadd.s64 b2, %2, %9;\n\tadd.s64 b3, %2, %10;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a2, b2, %3, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a3, b3, %3, p1;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB1), "n"(OB2), "n"(OB3)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+            "add.s64 a1, %1, %5;\n\tadd.s64 a2, %1, %6;\n\tadd.s64 a3, %1, %7;\n\t"
+            "add.s64 b1, %2, %8;\n\tadd.s64 b2, %2, %9;\n\tadd.s64 b3, %2, %10;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, p1;\n\t}" ::"r"(d),
+            "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB1), "n"(OB2), "n"(OB3)
+            : "memory");
+}
+
+template <int OA1, int OA2, int OA3, int OB1, int OB2, int OB3, bool F8>
+__device__ __forceinline__ void mma4_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    if (F8)
+        asm volatile(
+            "{\n\t.reg .pred p0, p1;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+            "add.u32 a1, %1, %5;\n\tadd.u32 a2, %1, %6;\n\tadd.u32 a3, %1, %7;\n\t"
+            "add.s64 b1, %2, %8;\n\tadd.s64 b2, %2, %9;\n\tadd.s64 b3, %2, %10;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a1], b1, %3, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a2], b2, %3, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [a3], b3, %3, p1;\n\t}" ::"r"(d),
+            "r"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB1), "n"(OB2), "n"(OB3)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p0, p1;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+            "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+            "add.u32 a1, %1, %5;\n\tadd.u32 a2, %1, %6;\n\tadd.u32 a3, %1, %7;\n\t"
+            "add.s64 b1, %2, %8;\n\tadd.s64 b2, %2, %9;\n\tadd.s64 b3, %2, %10;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, p1;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, p1;\n\t}" ::"r"(d),
+            "r"(a), "l"(b), "r"(idesc), "r"(accumulate), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB1), "n"(OB2), "n"(OB3)
+            : "memory");
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose
