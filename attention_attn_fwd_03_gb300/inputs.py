@@ -20,7 +20,13 @@ discuss -- prefill over BHSD tensors and one-token decode over a paged cache):
   unused table entries are -1.  K and V caches [num_pages, page_size, H, d]
   are N(0,1) bf16 drawn by a generator on ``device`` seeded with ``seed``;
   pool pages that no table entry references are filled with NaN so a stray
-  read poisons the output.
+  read poisons the output.  With grouped KV heads the caches hold H_kv heads
+  ([num_pages, page_size, H_kv, d]) and everything else is drawn the same way.
+* paged prefill chunks: the CPU generator draws the page permutation, then
+  per-request new-token counts q_len (uniform in [q_lo, q_hi]), then cached
+  prefix lengths (uniform in [ctx_lo, ctx_hi]), then q [total_q, H, d]
+  token-major; seq_len = prefix + q_len keys per request, pages assigned in
+  request order from the permutation; caches as for paged decode.
 """
 import math
 
@@ -48,26 +54,20 @@ def fp8_quantize(x):
     return y, float(1.0 / s)
 
 
-def paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192,
-             len_lo=512, len_hi=8192, seed=0, device="cpu", nan_fill_unused=True):
-    """Returns dict(q, k_cache, v_cache, block_table, seq_lens, used_pages)."""
-    if B * max_pages > num_pages:
-        raise ValueError("page pool smaller than B * max_pages")
-    if len_hi > max_pages * page_size or len_lo < 0 or len_lo > len_hi:
-        raise ValueError("length range does not fit the block table")
-    g = torch.Generator(device="cpu").manual_seed(seed)
-    perm = torch.randperm(num_pages, generator=g)
-    seq_lens = torch.randint(len_lo, len_hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
-    q = torch.randn((B, H, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+def _fill_tables(seq_lens, perm, max_pages, page_size):
+    B = seq_lens.shape[0]
     block_table = torch.full((B, max_pages), -1, dtype=torch.int32)
     cursor = 0
     for r in range(B):
         n = int(math.ceil(int(seq_lens[r]) / page_size))
         block_table[r, :n] = perm[cursor:cursor + n].to(torch.int32)
         cursor += n
-    used = perm[:cursor].clone()
+    return block_table, perm[:cursor].clone()
+
+
+def _caches(num_pages, page_size, H_kv, d, used, seed, device, nan_fill_unused):
     gd = torch.Generator(device=device).manual_seed(seed)
-    shape = (num_pages, page_size, H, d)
+    shape = (num_pages, page_size, H_kv, d)
     k_cache = torch.randn(shape, generator=gd, device=device, dtype=torch.bfloat16)
     v_cache = torch.randn(shape, generator=gd, device=device, dtype=torch.bfloat16)
     if nan_fill_unused:
@@ -77,8 +77,57 @@ def paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192,
         if idx.numel():
             k_cache.index_fill_(0, idx, float("nan"))
             v_cache.index_fill_(0, idx, float("nan"))
+    return k_cache, v_cache
+
+
+def paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192,
+             len_lo=512, len_hi=8192, seed=0, device="cpu", nan_fill_unused=True, H_kv=None):
+    """Returns dict(q, k_cache, v_cache, block_table, seq_lens, used_pages)."""
+    H_kv = H if H_kv is None else H_kv
+    if H_kv < 1 or H % H_kv:
+        raise ValueError("H_kv must divide H")
+    if B * max_pages > num_pages:
+        raise ValueError("page pool smaller than B * max_pages")
+    if len_hi > max_pages * page_size or len_lo < 0 or len_lo > len_hi:
+        raise ValueError("length range does not fit the block table")
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)
+    seq_lens = torch.randint(len_lo, len_hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    q = torch.randn((B, H, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    block_table, used = _fill_tables(seq_lens, perm, max_pages, page_size)
+    k_cache, v_cache = _caches(num_pages, page_size, H_kv, d, used, seed, device, nan_fill_unused)
     return dict(q=q.to(device), k_cache=k_cache, v_cache=v_cache,
                 block_table=block_table.to(device), seq_lens=seq_lens.to(device), used_pages=used)
+
+
+def paged_chunks(B=4, H=8, H_kv=2, d=128, page_size=64, max_pages=16, num_pages=128,
+                 q_lo=1, q_hi=256, ctx_lo=0, ctx_hi=512, seed=0, device="cpu", nan_fill_unused=True):
+    """Prefill chunks appended to cached prefixes over a paged cache.
+
+    Returns dict(q [total_q, H, d], cu_seqlens_q [B+1] int32, q_lens [B],
+    seq_lens [B] int32 (prefix + new tokens), block_table, k_cache, v_cache
+    [num_pages, page_size, H_kv, d], used_pages, max_q_len).
+    """
+    if H_kv < 1 or H % H_kv:
+        raise ValueError("H_kv must divide H")
+    if B * max_pages > num_pages:
+        raise ValueError("page pool smaller than B * max_pages")
+    if q_lo < 0 or q_lo > q_hi or ctx_lo < 0 or ctx_lo > ctx_hi or q_hi + ctx_hi > max_pages * page_size:
+        raise ValueError("length ranges do not fit the block table")
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    perm = torch.randperm(num_pages, generator=g)
+    q_lens = torch.randint(q_lo, q_hi + 1, (B,), generator=g, dtype=torch.int64)
+    ctx = torch.randint(ctx_lo, ctx_hi + 1, (B,), generator=g, dtype=torch.int64)
+    seq_lens = (ctx + q_lens).to(torch.int32)
+    cu = torch.zeros(B + 1, dtype=torch.int64)
+    cu[1:] = torch.cumsum(q_lens, 0)
+    total_q = int(cu[-1])
+    q = torch.randn((total_q, H, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    block_table, used = _fill_tables(seq_lens, perm, max_pages, page_size)
+    k_cache, v_cache = _caches(num_pages, page_size, H_kv, d, used, seed, device, nan_fill_unused)
+    return dict(q=q.to(device), cu_seqlens_q=cu.to(torch.int32).to(device), q_lens=q_lens,
+                seq_lens=seq_lens.to(device), block_table=block_table.to(device), k_cache=k_cache,
+                v_cache=v_cache, used_pages=used, max_q_len=int(q_lens.max()) if B else 0)
 
 
 def sample_rows(BH, Nq, n_random=4096, tile=128, seed=0):

@@ -11,6 +11,10 @@ numpy / torch CPU arrays into it.
 Parity status of each function (the pins live in tests/test_oracle_pins.py):
   attention      pinned (worked example, closed forms, tiled-vs-naive, mpmath)
   paged_decode   pinned (equal to attention on the gathered keys; table invariance)
+  paged_attention pinned (grouped heads equal multi-head attention on a cache
+                 whose KV heads are repeated; prefill chunks equal dense
+                 bottom-right causal attention on the gathered keys; one
+                 token per request equals paged_decode; closed forms)
   decode_elems   pinned (bf16 / e4m3fn codes against torch's conversions)
 """
 from .oracle import (  # noqa: F401
@@ -19,5 +23,6 @@ from .oracle import (  # noqa: F401
     build,
     decode_elems,
     default_threads,
+    paged_attention,
     paged_decode,
 )

@@ -37,6 +37,18 @@
  * same row computation with one query per request, where key t of request r
  * lives at cache[block_table[r][t / page_size]][t % page_size][h][:].
  *
+ * Paged attention in general (oracle_paged_attention) extends that to
+ *   - grouped KV heads: the cache holds H_kv heads, H_kv divides H, and query
+ *     head h reads KV head h / (H / H_kv) (H_kv = H is plain multi-head
+ *     attention, H_kv = 1 multi-query attention);
+ *   - several new query tokens per request (a prefill chunk appended to a
+ *     cached prefix): request r owns query tokens cu_q[r] .. cu_q[r+1]-1 of a
+ *     token-major q [total_q, H, d]; its keys are the seq_lens[r] cache
+ *     entries, the last q_len of which belong to the new tokens, so query i
+ *     of the request sits at position seq_lens[r] - q_len + i and, under the
+ *     causal mask, sees keys t <= that position (the bottom-right alignment
+ *     used for dense attention).
+ *
  * Input element types: float64, float32, bfloat16 bit patterns, e4m3fn bit
  * patterns.  bf16 and e4m3fn are decoded from their bit-level definitions.
  */
@@ -167,10 +179,11 @@ typedef struct {
     int64_t BH, Nq, Nk;
     int causal;
     const int64_t* rows; int64_t n_rows;
-    /* paged problem (used when paged != 0) */
+    /* paged problem (used when paged != 0); cu_q == NULL means one query
+     * token per request */
     int paged;
-    const int32_t* block_table; const int32_t* seq_lens;
-    int H, page_size, max_pages; int64_t num_pages;
+    const int32_t* block_table; const int32_t* seq_lens; const int32_t* cu_q;
+    int B, H, H_kv, page_size, max_pages; int64_t num_pages;
     /* outputs */
     double* o; double* lse; double* psum;
     /* work distribution and error reporting */
@@ -209,12 +222,26 @@ static void* worker(void* arg) {
             }
             for (j = 0; j < n; ++j) off[j] = (bh * jb->Nk + j) * d;
         } else {
-            int64_t req = r / jb->H, h = r % jb->H;
+            /* row r = (query token tok, query head h) of a token-major q */
+            int64_t tok = r / jb->H, h = r % jb->H;
+            int64_t req = tok, q_len = 1, i = 0;
+            if (jb->cu_q) { /* the request whose token range holds tok */
+                for (req = 0; req < jb->B; ++req)
+                    if (tok >= jb->cu_q[req] && tok < jb->cu_q[req + 1]) break;
+                q_len = jb->cu_q[req + 1] - jb->cu_q[req];
+                i = tok - jb->cu_q[req];
+            }
+            const int64_t kvh = h / (jb->H / jb->H_kv); /* grouped KV head */
             load_row(jb->q, jb->q_dt, r * d, d, jb->q_ds, qr);
-            n = jb->seq_lens[req];
+            const int64_t len = jb->seq_lens[req];
+            n = len;
             if (n < 0 || n > (int64_t)jb->max_pages * jb->page_size) {
                 __atomic_store_n(&jb->err, OR_BAD_PAGE, __ATOMIC_RELAXED);
                 n = 0;
+            } else if (jb->causal) {
+                n = len - q_len + i + 1; /* keys up to the query's own position */
+                if (n < 0) n = 0;
+                if (n > len) n = len;
             }
             for (j = 0; j < n; ++j) {
                 int64_t page = jb->block_table[req * jb->max_pages + j / jb->page_size];
@@ -223,7 +250,7 @@ static void* worker(void* arg) {
                     n = 0;
                     break;
                 }
-                off[j] = ((page * jb->page_size + j % jb->page_size) * jb->H + h) * d;
+                off[j] = ((page * jb->page_size + j % jb->page_size) * jb->H_kv + kvh) * d;
             }
         }
         attend_row(&jb->kv, qr, off, n, s, kr, jb->o + r * d, jb->lse + r,
@@ -304,9 +331,53 @@ int oracle_paged_decode(const void* q, int q_dt,
     jb.kv.v = v_cache; jb.kv.v_dt = kv_dt; jb.kv.v_ds = 1.0;
     jb.kv.d = d; jb.kv.scale = scale;
     jb.paged = 1;
-    jb.block_table = block_table; jb.seq_lens = seq_lens;
-    jb.H = H; jb.page_size = page_size; jb.max_pages = max_pages; jb.num_pages = num_pages;
+    jb.block_table = block_table; jb.seq_lens = seq_lens; jb.cu_q = NULL;
+    jb.B = B; jb.H = H; jb.H_kv = H;
+    jb.page_size = page_size; jb.max_pages = max_pages; jb.num_pages = num_pages;
     jb.n_rows = (int64_t)B * H;
+    jb.o = o; jb.lse = lse; jb.psum = psum;
+    return run_job(&jb, nthreads);
+}
+
+/* Paged attention with grouped KV heads and several query tokens per request.
+ *   q: [total_q, H, d] token-major; k_cache and v_cache: [num_pages,
+ *   page_size, H_kv, d] with H % H_kv == 0; block_table: [B, max_pages];
+ *   cu_q: [B + 1] non-decreasing token offsets with cu_q[0] = 0 and
+ *   cu_q[B] = total_q, or NULL for one query token per request (total_q = B);
+ *   seq_lens: [B] key counts, each >= the request's query count.
+ *   causal: query i of request r sees keys t <= seq_lens[r] - q_len_r + i.
+ *   o: [total_q*H, d], lse: [total_q*H], psum optional.  Errors as
+ *   oracle_paged_decode. */
+int oracle_paged_attention(const void* q, int q_dt,
+                           const void* k_cache, const void* v_cache, int kv_dt,
+                           const int32_t* block_table, const int32_t* cu_q, const int32_t* seq_lens,
+                           int B, int64_t total_q, int H, int H_kv, int d, int page_size, int max_pages,
+                           int64_t num_pages, double scale, int causal,
+                           double* o, double* lse, double* psum, int nthreads) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse) return OR_BAD_ARG;
+    if (!dtype_ok(q_dt) || !dtype_ok(kv_dt)) return OR_BAD_ARG;
+    if (B < 0 || total_q < 0 || H < 1 || H_kv < 1 || H % H_kv != 0 || d < 1 || d > 4096 ||
+        page_size < 1 || max_pages < 0 || num_pages < 0)
+        return OR_BAD_ARG;
+    if (cu_q) {
+        if (cu_q[0] != 0 || cu_q[B] != total_q) return OR_BAD_ARG;
+        for (int r = 0; r < B; ++r)
+            if (cu_q[r + 1] < cu_q[r]) return OR_BAD_ARG;
+    } else if (total_q != B) {
+        return OR_BAD_ARG;
+    }
+    job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.q_dt = q_dt; jb.q_ds = 1.0;
+    jb.kv.k = k_cache; jb.kv.k_dt = kv_dt; jb.kv.k_ds = 1.0;
+    jb.kv.v = v_cache; jb.kv.v_dt = kv_dt; jb.kv.v_ds = 1.0;
+    jb.kv.d = d; jb.kv.scale = scale;
+    jb.paged = 1;
+    jb.causal = causal;
+    jb.block_table = block_table; jb.seq_lens = seq_lens; jb.cu_q = cu_q;
+    jb.B = B; jb.H = H; jb.H_kv = H_kv;
+    jb.page_size = page_size; jb.max_pages = max_pages; jb.num_pages = num_pages;
+    jb.n_rows = total_q * H;
     jb.o = o; jb.lse = lse; jb.psum = psum;
     return run_job(&jb, nthreads);
 }

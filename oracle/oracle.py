@@ -45,6 +45,9 @@ def build(force=False):
             lib.oracle_paged_decode.restype = i
             lib.oracle_paged_decode.argtypes = [vp, i, vp, vp, i, vp, vp, i, i, i, i, i, i64,
                                                 dbl, vp, vp, vp, i]
+            lib.oracle_paged_attention.restype = i
+            lib.oracle_paged_attention.argtypes = [vp, i, vp, vp, i, vp, vp, vp, i, i64, i, i, i, i, i, i64,
+                                                   dbl, i, vp, vp, vp, i]
             lib.oracle_decode.restype = i
             lib.oracle_decode.argtypes = [vp, i, i64, vp]
             _lib = lib
@@ -161,6 +164,50 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, nthreads=Non
     _check(rc)
     res = (o.reshape(B, H, d), lse.reshape(B, H))
     return res + (psum.reshape(B, H),) if with_psum else res
+
+
+def paged_attention(q, k_cache, v_cache, block_table, seq_lens, scale, cu_seqlens_q=None, causal=False,
+                    nthreads=None, with_psum=False):
+    """Attention over a paged cache with grouped KV heads and several query
+    tokens per request.
+
+    q [total_q, H, d] token-major; k_cache, v_cache [num_pages, page_size,
+    H_kv, d] with H % H_kv == 0 (query head h reads KV head h // (H // H_kv));
+    block_table [B, max_pages] int32; seq_lens [B] int32 (keys per request,
+    the new tokens' keys last); cu_seqlens_q [B+1] int32 token offsets, or
+    None for one query token per request.  causal: query i of request r sees
+    keys t <= seq_lens[r] - q_len_r + i.  Returns (o [total_q,H,d],
+    lse [total_q,H]).
+    """
+    lib = build()
+    qa, qd = _as_raw(q)
+    ka, kd = _as_raw(k_cache)
+    va, vd = _as_raw(v_cache)
+    if kd != vd or ka.shape != va.shape:
+        raise OracleError("k_cache and v_cache must match in shape and type")
+    bt = np.ascontiguousarray(_to_numpy(block_table), dtype=np.int32)
+    sl = np.ascontiguousarray(_to_numpy(seq_lens), dtype=np.int32)
+    total_q, H, d = qa.shape
+    num_pages, page_size, H_kv, dc = ka.shape
+    B = sl.shape[0]
+    if dc != d or bt.shape[0] != B or H % H_kv != 0:
+        raise OracleError("shape mismatch")
+    cu = None
+    if cu_seqlens_q is not None:
+        cu = np.ascontiguousarray(_to_numpy(cu_seqlens_q), dtype=np.int32)
+        if cu.shape != (B + 1,):
+            raise OracleError("cu_seqlens_q must have B + 1 entries")
+    o = np.empty((total_q * H, d), dtype=np.float64)
+    lse = np.empty((total_q * H,), dtype=np.float64)
+    psum = np.empty((total_q * H,), dtype=np.float64) if with_psum else None
+    rc = lib.oracle_paged_attention(_ptr(qa), qd, _ptr(ka), _ptr(va), kd, _ptr(bt),
+                                    _ptr(cu) if cu is not None else None, _ptr(sl), B, total_q, H, H_kv, d,
+                                    page_size, bt.shape[1], num_pages, float(scale), int(bool(causal)),
+                                    _ptr(o), _ptr(lse), _ptr(psum) if with_psum else None,
+                                    int(nthreads or default_threads()))
+    _check(rc)
+    res = (o.reshape(total_q, H, d), lse.reshape(total_q, H))
+    return res + (psum.reshape(total_q, H),) if with_psum else res
 
 
 def decode_elems(x):

@@ -57,3 +57,32 @@ def test_sample_rows_cover_tile_edges():
     for h in range(3):
         for i in (0, 127, 128, 255, 256, 999, 872):
             assert h * 1000 + i in set(rows.tolist())
+
+
+def test_paged_chunk_inputs_structure():
+    p = inputs.paged_chunks(B=5, H=6, H_kv=2, d=8, page_size=4, max_pages=12, num_pages=60, q_lo=0, q_hi=9,
+                            ctx_lo=0, ctx_hi=30, seed=4)
+    cu, ql, sl, bt, kc, q = p["cu_seqlens_q"], p["q_lens"], p["seq_lens"], p["block_table"], p["k_cache"], p["q"]
+    assert cu.shape == (6,) and int(cu[0]) == 0 and torch.equal(cu[1:] - cu[:-1], ql.to(torch.int32))
+    assert q.shape == (int(cu[-1]), 6, 8) and kc.shape == (60, 4, 2, 8)
+    assert bool((sl >= ql.to(torch.int32)).all()) and int(sl.max()) <= 12 * 4
+    assert p["max_q_len"] == int(ql.max())
+    seen = []
+    for r in range(5):
+        n = math.ceil(int(sl[r]) / 4)
+        assert bool((bt[r, :n] >= 0).all()) and bool((bt[r, n:] == -1).all())
+        seen += bt[r, :n].tolist()
+    assert len(seen) == len(set(seen))
+    again = inputs.paged_chunks(B=5, H=6, H_kv=2, d=8, page_size=4, max_pages=12, num_pages=60, q_lo=0, q_hi=9,
+                                ctx_lo=0, ctx_hi=30, seed=4)
+    assert torch.equal(again["q"], q) and torch.equal(again["block_table"], bt)
+
+
+def test_grouped_cache_keeps_the_draw_order():
+    """Grouped KV heads change only the cache shape: table, lengths and q are
+    the multi-head recipe's."""
+    a = inputs.paged_kv(B=3, H=4, d=8, page_size=4, max_pages=4, num_pages=16, len_lo=1, len_hi=16, seed=5)
+    b = inputs.paged_kv(B=3, H=4, d=8, page_size=4, max_pages=4, num_pages=16, len_lo=1, len_hi=16, seed=5,
+                        H_kv=2)
+    assert torch.equal(a["q"], b["q"]) and torch.equal(a["block_table"], b["block_table"])
+    assert b["k_cache"].shape == (16, 4, 2, 8)

@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import oracle
+from attention_attn_fwd_03_gb300 import inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -397,3 +398,94 @@ def test_paged_bad_page_is_reported():
     bt[r, 0] = p["k_cache"].shape[0]  # one past the pool
     with pytest.raises(oracle.OracleError):
         oracle.paged_decode(p["q"], p["k_cache"], p["v_cache"], bt, p["seq_lens"], scale=0.3)
+
+
+# ---------------------------------------------------------------- paged attention: grouped heads, chunks
+
+def _gather(cache, bt, r, n, page):
+    """Keys 0..n-1 of request r as [heads, n, d] (test-side gather)."""
+    rows = [cache[int(bt[r, t // page]), t % page] for t in range(n)]
+    if not rows:
+        return cache.new_zeros((cache.shape[2], 0, cache.shape[3]))
+    return torch.stack(rows, dim=1)
+
+
+@pytest.mark.parametrize("H,H_kv", [(8, 2), (8, 1), (6, 3)])
+def test_grouped_heads_equal_multihead_on_repeated_cache(H, H_kv):
+    """Grouped-query attention is multi-head attention in which the KV head of
+    group g serves query heads g*G .. g*G+G-1 (G = H / H_kv): on a cache whose
+    heads are repeated G times in that order the two agree exactly.  A head
+    map other than h // G (e.g. h % H_kv) fails this."""
+    p = inputs.paged_kv(B=5, H=H, d=16, page_size=4, max_pages=6, num_pages=40, len_lo=0, len_hi=24,
+                        seed=11, H_kv=H_kv)
+    G = H // H_kv
+    kc_rep = p["k_cache"].repeat_interleave(G, dim=2)
+    vc_rep = p["v_cache"].repeat_interleave(G, dim=2)
+    o1, l1 = oracle.paged_attention(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], 0.25)
+    o2, l2 = oracle.paged_decode(p["q"], kc_rep, vc_rep, p["block_table"], p["seq_lens"], 0.25)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert np.all(np.isfinite(o1))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_chunks_equal_dense_attention_per_request(causal):
+    """A prefill chunk of q_len new tokens over seq_len cached keys is dense
+    attention with Nq = q_len, Nk = seq_len for each request, with the
+    bottom-right causal alignment ([P3] section 7.3's lower-triangular mask
+    on the last q_len rows of the full square)."""
+    page = 4
+    p = inputs.paged_chunks(B=4, H=4, H_kv=2, d=8, page_size=page, max_pages=12, num_pages=60, q_lo=0, q_hi=7,
+                            ctx_lo=0, ctx_hi=30, seed=12)
+    q, cu, sl, bt = p["q"], p["cu_seqlens_q"], p["seq_lens"], p["block_table"]
+    o, lse = oracle.paged_attention(q, p["k_cache"], p["v_cache"], bt, sl, 0.3, cu_seqlens_q=cu, causal=causal)
+    G = 2
+    for r in range(4):
+        a, b = int(cu[r]), int(cu[r + 1])
+        if a == b:
+            continue
+        n = int(sl[r])
+        kr = _gather(p["k_cache"], bt, r, n, page).repeat_interleave(G, dim=0)  # [H, n, d]
+        vr = _gather(p["v_cache"], bt, r, n, page).repeat_interleave(G, dim=0)
+        qd = q[a:b].transpose(0, 1).contiguous()  # [H, q_len, d]
+        od, ld = oracle.attention(qd, kr, vr, scale=0.3, causal=causal)
+        assert np.array_equal(o[a:b], od.transpose(1, 0, 2)) and np.array_equal(lse[a:b], ld.T)
+
+
+def test_one_token_per_request_equals_decode():
+    """cu_seqlens_q = 0, 1, ..., B with the causal mask: each request's single
+    query sits at the last position and sees every cached key."""
+    p = inputs.paged_kv(B=6, H=4, d=16, page_size=8, max_pages=4, num_pages=30, len_lo=1, len_hi=32, seed=13)
+    cu = torch.arange(7, dtype=torch.int32)
+    o1, l1 = oracle.paged_attention(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], 0.2,
+                                    cu_seqlens_q=cu, causal=True)
+    o2, l2 = oracle.paged_decode(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], 0.2)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_zero_query_chunk_gives_prefix_means():
+    """Closed form: with q = 0 every visible key has probability 1/n, so under
+    the causal mask query i of a request with q_len new tokens over seq_len
+    keys returns the mean of the first seq_len - q_len + i + 1 value rows and
+    lse = ln(seq_len - q_len + i + 1)."""
+    page = 4
+    p = inputs.paged_chunks(B=3, H=2, H_kv=1, d=4, page_size=page, max_pages=8, num_pages=30, q_lo=1, q_hi=5,
+                            ctx_lo=0, ctx_hi=20, seed=14)
+    q = torch.zeros_like(p["q"])
+    cu, sl, bt = p["cu_seqlens_q"], p["seq_lens"], p["block_table"]
+    o, lse = oracle.paged_attention(q, p["k_cache"], p["v_cache"], bt, sl, 1.0, cu_seqlens_q=cu, causal=True)
+    for r in range(3):
+        a, b = int(cu[r]), int(cu[r + 1])
+        n_len = int(sl[r])
+        for i in range(b - a):
+            n = n_len - (b - a) + i + 1
+            vals = np.array([[float(x) for x in p["v_cache"][int(bt[r, t // page]), t % page, 0]] for t in range(n)])
+            for h in range(2):
+                assert np.allclose(o[a + i, h], vals.mean(axis=0), rtol=0, atol=1e-14)
+                assert abs(lse[a + i, h] - math.log(n)) < 1e-14
+
+
+def test_paged_attention_rejects_bad_offsets():
+    p = inputs.paged_kv(B=2, H=2, d=4, page_size=4, max_pages=2, num_pages=8, len_lo=1, len_hi=8, seed=15)
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_attention(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], 1.0,
+                               cu_seqlens_q=torch.tensor([0, 2, 1], dtype=torch.int32))
