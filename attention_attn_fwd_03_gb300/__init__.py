@@ -6,10 +6,13 @@ PyTorch fallback, and every call raises if the library is missing.
 
 Two levels:
   * ``attn_fwd``, ``attn_fwd_fp8``, ``attn_paged_decode``,
-    ``attn_paged_decode_workspace_size``, ``attn_device_status``,
-    ``attn_status_string``: the C entry points, same names and argument
-    order, taking raw device pointers (ints) and a stream handle (int).
-  * ``fwd``, ``fwd_fp8``, ``paged_decode``: take torch CUDA tensors, allocate
+    ``attn_paged_decode_workspace_size``, ``attn_paged_decode_noalloc``,
+    ``attn_paged_fwd``, ``attn_paged_fwd_workspace_size``,
+    ``attn_device_status``, ``attn_status_string``: the C entry points, same
+    names and argument order, taking raw device pointers (ints) and a stream
+    handle (int).
+  * ``fwd``, ``fwd_fp8``, ``paged_decode``, ``paged_fwd``: take torch CUDA
+    tensors, allocate
     outputs with torch when none are given, call the C entry point on the
     current stream and raise ``AttnError`` on a non-zero status.
 """
@@ -71,6 +74,11 @@ def lib():
             L.attn_paged_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp, sz, vp]
             L.attn_paged_decode_noalloc.restype = i
             L.attn_paged_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp, vp]
+            L.attn_paged_fwd_workspace_size.restype = sz
+            L.attn_paged_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+            L.attn_paged_fwd.restype = i
+            L.attn_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, sz,
+                                         vp]
             L.attn_device_status.restype = i
             L.attn_device_status.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -107,6 +115,18 @@ def attn_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, B, H, 
     scratch array; allocates nothing (see include/attn.h for its limits)."""
     return lib().attn_paged_decode_noalloc(q, k_cache, v_cache, block_table, seq_lens, B, H, d, page_size,
                                            max_pages_per_seq, num_pages, scale, o, lse, stream)
+
+
+def attn_paged_fwd_workspace_size(B, total_q, max_q_len, H, H_kv, d, page_size, max_pages_per_seq):
+    return lib().attn_paged_fwd_workspace_size(B, total_q, max_q_len, H, H_kv, d, page_size, max_pages_per_seq)
+
+
+def attn_paged_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, B, total_q, max_q_len, H, H_kv, d,
+                   page_size, max_pages_per_seq, num_pages, scale, causal, o, lse, workspace, workspace_bytes,
+                   stream):
+    return lib().attn_paged_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, B, total_q, max_q_len,
+                                H, H_kv, d, page_size, max_pages_per_seq, num_pages, scale, causal, o, lse,
+                                workspace, workspace_bytes, stream)
 
 
 def attn_device_status(stream):
@@ -226,6 +246,55 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, out=Non
                            lse.data_ptr() if lse is not None else None, workspace.data_ptr(), workspace.numel(),
                            _stream(stream))
     _raise(st, "attn_paged_decode")
+    return out, lse
+
+
+def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q=None, max_q_len=None, causal=False,
+              scale=None, out=None, lse=None, workspace=None, return_lse=True, stream=None):
+    """Tensor-core attention over a paged cache with grouped KV heads.
+
+    q bf16 [total_q, H, d] token-major; caches bf16 [num_pages, page_size,
+    H_kv, d]; block_table int32 [B, max_pages]; seq_lens int32 [B];
+    cu_seqlens_q int32 [B+1] (None: one query token per request, q [B, H, d]).
+    max_q_len is the largest per-request token count (read from
+    cu_seqlens_q, with a device-to-host copy, when not given).
+    Returns (o bf16 like q, lse fp32 [total_q, H]).
+    """
+    torch = _torch()
+    total_q, H, d = q.shape
+    num_pages, page_size, H_kv = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    B, max_pages = block_table.shape
+    _check(q, "q", torch.bfloat16)
+    _check(k_cache, "k_cache", torch.bfloat16, (num_pages, page_size, H_kv, d))
+    _check(v_cache, "v_cache", torch.bfloat16, (num_pages, page_size, H_kv, d))
+    _check(block_table, "block_table", torch.int32, (B, max_pages))
+    _check(seq_lens, "seq_lens", torch.int32, (B,))
+    if cu_seqlens_q is not None:
+        _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, (B + 1,))
+        if max_q_len is None:
+            max_q_len = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
+    else:
+        max_q_len = 1
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, (total_q, H, d))
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, H), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (total_q, H))
+    ws_bytes = attn_paged_fwd_workspace_size(B, total_q, max_q_len, H, H_kv, d, page_size, max_pages)
+    if ws_bytes > 0 and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    if workspace is not None:
+        _check(workspace, "workspace", torch.uint8)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    st = attn_paged_fwd(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                        cu_seqlens_q.data_ptr() if cu_seqlens_q is not None else None, seq_lens.data_ptr(), B,
+                        total_q, max_q_len, H, H_kv, d, page_size, max_pages, num_pages, sc, int(bool(causal)),
+                        out.data_ptr(), lse.data_ptr() if lse is not None else None,
+                        workspace.data_ptr() if workspace is not None else None,
+                        workspace.numel() if workspace is not None else 0, _stream(stream))
+    _raise(st, "attn_paged_fwd")
     return out, lse
 
 

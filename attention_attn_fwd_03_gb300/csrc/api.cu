@@ -124,6 +124,37 @@ attn_status_t prefill(const void* q, const void* k, const void* v, void* o, floa
     return from_cuda(launch_prefill(d, fp8, p, grid, static_cast<cudaStream_t>(stream)));
 }
 
+bool pow2_in(int x, int lo, int hi) { return x >= lo && x <= hi && (x & (x - 1)) == 0; }
+
+// Checks shared by the paged size query and the paged call; returns ATTN_OK
+// or the status to report.
+attn_status_t paged_sizes_ok(int B, int total_q, int max_q_len, int H, int H_kv, int d, int page_size,
+                             int max_pages) {
+    if (B < 1 || total_q < 1 || max_q_len < 1 || max_q_len > total_q || H < 1 || H_kv < 1 || max_pages < 1)
+        return ATTN_ERR_INVALID_ARG;
+    if (H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+    if (H / H_kv > 128 || (d != 64 && d != 128) || !pow2_in(page_size, 8, 1024)) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)max_pages * page_size > 0x7fffffffLL || (long long)B * max_pages > 0x7fffffffLL ||
+        (long long)total_q * H > 0x7fffffffLL)
+        return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+// Q map over [total_q, H, d]: box (64 elements, G heads, T tokens).  Cache
+// map over [slots, H_kv, d]: box (64 elements, 1 head, R rows).  Both with
+// 128-byte swizzle and zero fill outside the tensor.
+bool make_paged_map(CUtensorMap* map, const void* base, int d, long long heads, long long rows, int box_heads,
+                    int box_rows) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 // Device address of the calling device's status word (set-up on first use).
@@ -204,6 +235,77 @@ attn_status_t attn_paged_decode(const void* q, const void* k_cache, const void* 
     p.max_splits = pl.max_splits;
     p.c_scale = scale * 1.4426950408889634f;
     return from_cuda(launch_paged_decode(d, p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t attn_paged_fwd_workspace_size(int B, int total_q, int max_q_len, int H, int H_kv, int d, int page_size,
+                                     int max_pages_per_seq) {
+    if (paged_sizes_ok(B, total_q, max_q_len, H, H_kv, d, page_size, max_pages_per_seq) != ATTN_OK) return 0;
+    return paged_plan(total_q, max_q_len, B, H, H_kv, d, page_size, max_pages_per_seq).workspace_bytes;
+}
+
+attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                             const int32_t* cu_seqlens_q, const int32_t* seq_lens, int B, int total_q,
+                             int max_q_len, int H, int H_kv, int d, int page_size, int max_pages_per_seq,
+                             int num_pages, float scale, int causal, void* o, float* lse, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o) return ATTN_ERR_INVALID_ARG;
+    if (!cu_seqlens_q && (total_q != B || max_q_len != 1)) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = paged_sizes_ok(B, total_q, max_q_len, H, H_kv, d, page_size, max_pages_per_seq);
+    if (st != ATTN_OK) return st;
+    if (num_pages < 1 || (long long)num_pages * page_size > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    auto a4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
+    if (!a4(block_table) || !a4(seq_lens) || (cu_seqlens_q && !a4(cu_seqlens_q)) || (lse && !a4(lse)))
+        return ATTN_ERR_INVALID_ARG;
+    const PagedPlan pl = paged_plan(total_q, max_q_len, B, H, H_kv, d, page_size, max_pages_per_seq);
+    if (pl.n_units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (pl.workspace_bytes > 0 && (!workspace || workspace_bytes < pl.workspace_bytes || !aligned16(workspace)))
+        return ATTN_ERR_WORKSPACE;
+
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+
+    PagedParams p;
+    std::memset(&p, 0, sizeof p);
+    const long long slots = (long long)num_pages * page_size;
+    const int R = page_size < 128 ? page_size : 128;
+    if (!make_paged_map(&p.tm_q, q, d, H, total_q, pl.G, pl.T) ||
+        !make_paged_map(&p.tm_k, k_cache, d, H_kv, slots, 1, R) ||
+        !make_paged_map(&p.tm_v, v_cache, d, H_kv, slots, 1, R))
+        return ATTN_ERR_CUDA;
+    p.block_table = block_table;
+    p.cu_q = cu_seqlens_q;
+    p.seq_lens = seq_lens;
+    p.o = static_cast<uint16_t*>(o);
+    p.lse = lse;
+    if (pl.workspace_bytes > 0) {
+        p.part_o = static_cast<float*>(workspace);
+        p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + (pl.workspace_bytes - pl.part_ml_bytes));
+    }
+    p.status = ds->status;
+    p.B = B;
+    p.H = H;
+    p.H_kv = H_kv;
+    p.G = pl.G;
+    p.T = pl.T;
+    p.total_q = total_q;
+    p.max_q_len = max_q_len;
+    p.n_qt = pl.n_qt;
+    p.page_size = page_size;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.rows_per_box = R;
+    p.causal = causal;
+    p.n_splits = pl.n_splits;
+    p.split_blocks = pl.split_blocks;
+    p.n_units = (int)pl.n_units;
+    p.q_tile_bytes = (uint32_t)(d / 64) * (uint32_t)(pl.G * pl.T) * 128u;
+    p.c_scale = scale * 1.4426950408889634f;
+    const int grid = pl.n_units < ds->sm_count ? (int)pl.n_units : ds->sm_count;  // persistent: one CTA per SM
+    return from_cuda(launch_paged(d, p, grid, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status_t attn_device_status(void* stream) {

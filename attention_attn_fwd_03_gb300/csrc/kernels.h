@@ -60,6 +60,44 @@ DecodePlan decode_plan(int B, int H, int d, int page_size, int max_pages);
 
 cudaError_t launch_paged_decode(int d, const DecodeParams& p, cudaStream_t stream);
 
+// Paged attention on the tensor cores (grouped-query decode, prefill chunks
+// over a paged cache).  A query tile packs T tokens x G query heads of one KV
+// head into its 128 rows (row = t * G + g).
+struct PagedParams {
+    CUtensorMap tm_q;  // q [total_q, H, d]: dims (d, H, total_q), box (64, G, T), 128-B swizzle
+    CUtensorMap tm_k;  // cache [num_pages * page_size, H_kv, d]: dims (d, H_kv, slots), box (64, 1, R)
+    CUtensorMap tm_v;
+    const int32_t* block_table;  // [B, max_pages]
+    const int32_t* cu_q;         // [B + 1] token offsets, or nullptr: one token per request
+    const int32_t* seq_lens;     // [B] keys per request
+    uint16_t* o;                 // bf16 [total_q, H, d]
+    float* lse;                  // [total_q, H] or nullptr
+    float* part_o;               // [total_q * H, n_splits, d] unnormalised partial O (n_splits > 1)
+    float* part_ml;              // [total_q * H, n_splits, 2] (m in log2 units, l)
+    unsigned* status;
+    int B, H, H_kv, G, T;        // T = tokens per query tile
+    int total_q, max_q_len, n_qt;
+    int page_size, max_pages, num_pages, rows_per_box;  // rows_per_box = min(page_size, 128)
+    int causal;
+    int n_splits, split_blocks;  // split s covers KV blocks [s, s + 1) * split_blocks
+    int n_units;                 // B * H_kv * n_qt * n_splits
+    uint32_t q_tile_bytes;       // bytes one Q tile load delivers
+    float c_scale;               // scale * log2(e)
+};
+
+constexpr int kPagedThreads = 192;  // TMA warp + MMA warp + one softmax warpgroup
+
+// Split plan shared by the size query and the launcher.
+struct PagedPlan {
+    int G, T, n_qt, n_splits, split_blocks;
+    long long n_units;
+    size_t part_o_bytes, part_ml_bytes, workspace_bytes;  // workspace_bytes == 0: no split
+};
+PagedPlan paged_plan(int total_q, int max_q_len, int B, int H, int H_kv, int d, int page_size, int max_pages);
+
+int paged_smem_bytes(int d);
+cudaError_t launch_paged(int d, const PagedParams& p, int grid, cudaStream_t stream);
+
 }  // namespace attn
 
 #include "attn.h"

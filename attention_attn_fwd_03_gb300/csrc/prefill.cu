@@ -41,6 +41,7 @@
 // holds for any common reference point), and p stays <= 2^kTau.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tile_mma.cuh"
 
 namespace attn {
 
@@ -57,18 +58,11 @@ struct Cfg {
     static constexpr int NPANEL = D / PANEL;       // panels per row
     static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B
     static constexpr int TILE_BYTES = NPANEL * PANEL_BYTES;
-    static constexpr int MMA_K = FP8 ? 32 : 16;    // K per tcgen05.mma (32 bytes)
-    static constexpr int S_STEPS = D / MMA_K;
-    static constexpr int PV_STEPS = BN / MMA_K;
     static constexpr int NST = (D == 128 && !FP8) ? 4 : 8;  // K/V ring stages
     static constexpr int OST_WARP_BYTES = 2 * 32 * 64;      // two 32x32 bf16 staging buffers per warp
     __host__ __device__ static constexpr uint32_t tm_s(int t) { return t ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t tm_o(int t) { return 256u + (t ? (uint32_t)D : 0u); }
     static constexpr uint32_t TM_COLS = 512;
-    static constexpr uint32_t P_STEP_COLS = MMA_K * EB / 4;  // TMEM columns per PV step
-    static constexpr uint32_t FMT = FP8 ? 0u : 1u;           // e4m3 / bf16
-    static constexpr uint32_t ID_S = idesc_make(128, 128, FMT, false, false);
-    static constexpr uint32_t ID_PV = idesc_make(128, D, FMT, false, true);
     // shared memory map (offsets from a 1024-byte aligned base)
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_KV = OFF_Q + 2 * TILE_BYTES;
@@ -150,18 +144,6 @@ __device__ __forceinline__ int next_unit(const PrefillParams& p, int& round_) {
     }
 }
 
-// Wait that ignores the abort flag (used only to drain in-flight async work
-// before the CTA releases its shared and tensor memory); bounded in time.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
-    const unsigned long long t0 = globaltimer();
-    while (!bar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kWaitLimitNs) {
-            atomicOr(status, 1u << kStatusTimeout);
-            return;
-        }
-    }
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -231,35 +213,6 @@ __device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars&
 }
 
 // ---------------------------------------------------------------- MMA issuers
-
-// S = Q K^T: S_STEPS MMAs along d.  a0 / b0 are the descriptors of the Q and K
-// tiles; the k-th step starts (k / 4) panels and (k % 4) * 32 bytes further
-// (the descriptor's start-address field holds byte address >> 4).
-template <int D, bool FP8>
-__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint64_t a0, uint64_t b0) {
-    using C = Cfg<D, FP8>;
-    // four 32-byte K steps per 128-byte panel; next panel PANEL_BYTES further
-#pragma unroll
-    for (int g = 0; g < C::S_STEPS / 4; ++g) {
-        const uint64_t po = (uint64_t)((g * C::PANEL_BYTES) >> 4);
-        mma4_ss<2, 4, 6, 2, 4, 6, FP8>(d_tmem, a0 + po, b0 + po, C::ID_S, g > 0 ? 1u : 0u);
-    }
-}
-
-// O += P V: PV_STEPS MMAs along the keys; P from tensor memory (P_STEP_COLS
-// columns per step), b0 the descriptor of the MN-major V tile (step s starts
-// s * MMA_K rows, i.e. s * MMA_K * 128 bytes, further).
-template <int D, bool FP8>
-__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint64_t b0, bool accumulate) {
-    using C = Cfg<D, FP8>;
-    constexpr int PC = (int)C::P_STEP_COLS;
-    constexpr int VB = (C::MMA_K * 128) >> 4;
-#pragma unroll
-    for (int g = 0; g < C::PV_STEPS / 4; ++g)
-        mma4_ts<PC, 2 * PC, 3 * PC, VB, 2 * VB, 3 * VB, FP8>(o_tmem, p_tmem + (uint32_t)(4 * g * PC),
-                                                           b0 + (uint64_t)(4 * g * VB), C::ID_PV,
-                                                           (accumulate || g > 0) ? 1u : 0u);
-}
 
 // MMA issuers: warp t issues query tile t's GEMMs.  The two issuers take
 // strict turns through the turn[] barriers, one group of GEMMs per turn, so

@@ -98,6 +98,18 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     }
 }
 
+// Wait that ignores the abort flag (used only to drain in-flight async work
+// before the CTA releases its shared and tensor memory); bounded in time.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+    const unsigned long long t0 = globaltimer();
+    while (!bar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(status, 1u << kStatusTimeout);
+            return;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {

@@ -141,12 +141,59 @@ attn_status_t attn_paged_decode_noalloc(const void* q, const void* k_cache, cons
                                         int B, int H, int d, int page_size, int max_pages_per_seq,
                                         int num_pages, float scale, void* o, float* lse, void* stream);
 
+/* Bytes of device workspace attn_paged_fwd needs for these sizes; 0 when no
+ * workspace is needed (every unit covers all of its keys) or the sizes are
+ * invalid.  The workspace holds per-split partials (unnormalised O, m, l). */
+size_t attn_paged_fwd_workspace_size(int B, int total_q, int max_q_len, int H, int H_kv, int d, int page_size,
+                                     int max_pages_per_seq);
+
+/* Attention over a paged KV cache on the tensor cores, for grouped-query
+ * decode and for prefill chunks appended to cached prefixes.
+ * The cache is the page-table layout of "FlashAttention V3 实战", section 3.2,
+ * with H_kv KV heads per slot; query head h reads KV head h / (H / H_kv)
+ * (grouped-query attention; H_kv = H is multi-head, H_kv = 1 multi-query).
+ * The arithmetic is that of attn_fwd: online softmax (Capstone page, section
+ * 2.2) with one final division, and the (m, l, O) merge of section 2.2 step 4
+ * when a request's keys are split over several CTAs.
+ *   q: bf16 [total_q, H, d], token-major: request r owns query tokens
+ *     cu_seqlens_q[r] .. cu_seqlens_q[r+1]-1
+ *   k_cache, v_cache: bf16 [num_pages, page_size, H_kv, d]
+ *   block_table: int32 [B, max_pages_per_seq], physical page ids
+ *   cu_seqlens_q: int32 [B + 1] device offsets, non-decreasing, first 0 and
+ *     last total_q, each request at most max_q_len tokens; or NULL for one
+ *     query token per request (then total_q == B and max_q_len == 1)
+ *   seq_lens: int32 [B] device key counts; the request's query tokens are its
+ *     last q_len keys (their K/V already written to the cache), so query i of
+ *     request r sits at position seq_lens[r] - q_len_r + i; key t lives at
+ *     cache[block_table[r][t / page_size]][t % page_size]
+ *   causal: 1 = query at position P sees keys t <= P (the bottom-right
+ *     aligned lower triangle of attn_fwd); 0 = every query sees all keys
+ *   o: bf16 [total_q, H, d]; lse: fp32 [total_q, H] or NULL
+ *   workspace: at least attn_paged_fwd_workspace_size(...) bytes (may be NULL
+ *     when that is 0), caller-owned, contents need no initialisation
+ *   d in {64, 128}; page_size a power of two in [8, 1024]; H % H_kv == 0 and
+ *   H / H_kv <= 128.
+ * A query with no visible key gets O = 0 and lse = -inf.
+ * Device-side data is the caller's contract: offsets out of range drop that
+ * request's queries (its rows are not written), a length outside
+ * [0, max_pages_per_seq * page_size] is clamped, a page id outside
+ * [0, num_pages) reads zeros; each sets the device status word to
+ * ATTN_ERR_DEVICE_DATA, after which the call's results are undefined.
+ * Errors: ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED / ATTN_ERR_WORKSPACE
+ * before any launch; ATTN_ERR_CUDA when a launch fails. */
+attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_table, const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                             int B, int total_q, int max_q_len, int H, int H_kv, int d, int page_size,
+                             int max_pages_per_seq, int num_pages, float scale, int causal,
+                             void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then reads and clears the calling device's status
  * word.  Kernels set it when a bounded internal wait gives up
  * (ATTN_ERR_TIMEOUT; the kernel then returns early and its outputs are
  * undefined) or when paged-decode device data is out of range
- * (ATTN_ERR_DEVICE_DATA).  While the word is set, prefill kernels return
- * without work, so check it after any call whose result matters.
+ * (ATTN_ERR_DEVICE_DATA).  While the word is set, the attn_fwd, attn_fwd_fp8
+ * and attn_paged_fwd kernels return without work, so check it after any
+ * call whose result matters.
  * Returns ATTN_OK, one of those two codes, or ATTN_ERR_CUDA. */
 attn_status_t attn_device_status(void* stream);
 

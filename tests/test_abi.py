@@ -27,6 +27,7 @@ def _declared():
 def test_header_declares_the_entry_points():
     assert _declared() == sorted(["attn_fwd", "attn_fwd_fp8", "attn_paged_decode",
                                   "attn_paged_decode_workspace_size", "attn_paged_decode_noalloc",
+                                  "attn_paged_fwd", "attn_paged_fwd_workspace_size",
                                   "attn_device_status", "attn_status_string"])
 
 
@@ -115,3 +116,34 @@ def test_library_has_no_oracle_dependency():
     for f in ("__init__.py", "_build.py", "inputs.py"):
         text = open(os.path.join(ROOT, "attention_attn_fwd_03_gb300", f), encoding="utf-8").read()
         assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_paged_fwd_workspace_size_query(L):
+    # one token per request over 8192-key caches: runs of 8 KV blocks, 8 splits
+    ws = attn.attn_paged_fwd_workspace_size(64, 64, 1, 32, 8, 128, 64, 128)
+    assert ws >= 64 * 32 * 8 * 130 * 4
+    # everything fits one split: no workspace
+    assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 2, 128, 64, 16) == 0
+    assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 3, 128, 64, 16) == 0  # H % H_kv != 0
+    assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 2, 128, 48, 16) == 0  # page size not a power of two
+    assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 512, 2, 128, 64, 16) == 0  # 256 heads per group
+    assert attn.attn_paged_fwd_workspace_size(4, 4, 5, 8, 2, 128, 64, 16) == 0  # max_q_len > total_q
+
+
+def test_paged_fwd_validation(L):
+    base = dict(q=FAKE, k_cache=FAKE, v_cache=FAKE, block_table=FAKE, cu_seqlens_q=None, seq_lens=FAKE, B=4,
+                total_q=4, max_q_len=1, H=8, H_kv=2, d=128, page_size=64, max_pages_per_seq=16, num_pages=64,
+                scale=0.088, causal=0, o=FAKE, lse=None, workspace=None, workspace_bytes=0, stream=None)
+    assert attn.attn_paged_fwd(**dict(base, H_kv=3)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_paged_fwd(**dict(base, total_q=5)) == attn.ATTN_ERR_INVALID_ARG  # no offsets: one token each
+    assert attn.attn_paged_fwd(**dict(base, page_size=48)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_paged_fwd(**dict(base, d=96)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_paged_fwd(**dict(base, causal=2)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_paged_fwd(**dict(base, q=FAKE + 8)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_paged_fwd(**dict(base, num_pages=0)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_paged_fwd(**dict(base, seq_lens=None)) == attn.ATTN_ERR_INVALID_ARG
+    long = dict(base, max_pages_per_seq=128, num_pages=1024)
+    ws = attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 2, 128, 64, 128)
+    assert ws > 0
+    assert attn.attn_paged_fwd(**long) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_paged_fwd(**dict(long, workspace=FAKE, workspace_bytes=ws - 1)) == attn.ATTN_ERR_WORKSPACE
