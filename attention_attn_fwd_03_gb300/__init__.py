@@ -283,17 +283,17 @@ def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q=None, max
     if lse is not None:
         _check(lse, "lse", torch.float32, (total_q, H))
     ws_bytes = attn_paged_fwd_workspace_size(B, total_q, max_q_len, H, H_kv, d, page_size, max_pages)
-    if ws_bytes > 0 and workspace is None:
+    if ws_bytes == 0:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "attn_paged_fwd_workspace_size")
+    if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    if workspace is not None:
-        _check(workspace, "workspace", torch.uint8)
+    _check(workspace, "workspace", torch.uint8)
     sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
     st = attn_paged_fwd(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
                         cu_seqlens_q.data_ptr() if cu_seqlens_q is not None else None, seq_lens.data_ptr(), B,
                         total_q, max_q_len, H, H_kv, d, page_size, max_pages, num_pages, sc, int(bool(causal)),
-                        out.data_ptr(), lse.data_ptr() if lse is not None else None,
-                        workspace.data_ptr() if workspace is not None else None,
-                        workspace.numel() if workspace is not None else 0, _stream(stream))
+                        out.data_ptr(), lse.data_ptr() if lse is not None else None, workspace.data_ptr(),
+                        workspace.numel(), _stream(stream))
     _raise(st, "attn_paged_fwd")
     return out, lse
 

@@ -261,8 +261,7 @@ attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_c
         return ATTN_ERR_INVALID_ARG;
     const PagedPlan pl = paged_plan(total_q, max_q_len, B, H, H_kv, d, page_size, max_pages_per_seq);
     if (pl.n_units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
-    if (pl.workspace_bytes > 0 && (!workspace || workspace_bytes < pl.workspace_bytes || !aligned16(workspace)))
-        return ATTN_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < pl.workspace_bytes || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
 
     DeviceState* ds = nullptr;
     st = device_state(&ds);
@@ -281,9 +280,12 @@ attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_c
     p.seq_lens = seq_lens;
     p.o = static_cast<uint16_t*>(o);
     p.lse = lse;
-    if (pl.workspace_bytes > 0) {
-        p.part_o = static_cast<float*>(workspace);
-        p.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) + (pl.workspace_bytes - pl.part_ml_bytes));
+    p.sched = static_cast<int*>(workspace);
+    char* ws = static_cast<char*>(workspace);
+    p.sched_list = reinterpret_cast<int4*>(ws + pl.list_offset);
+    if (pl.n_splits > 1) {
+        p.part_o = reinterpret_cast<float*>(ws + pl.part_o_offset);
+        p.part_ml = reinterpret_cast<float*>(ws + pl.part_ml_offset);
     }
     p.status = ds->status;
     p.B = B;

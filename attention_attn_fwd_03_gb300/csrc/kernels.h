@@ -75,6 +75,8 @@ struct PagedParams {
     float* part_o;               // [total_q * H, n_splits, d] unnormalised partial O (n_splits > 1)
     float* part_ml;              // [total_q * H, n_splits, 2] (m in log2 units, l)
     unsigned* status;
+    int* sched;                  // [0] fetch counter, [1] list length (written by the schedule pass)
+    int4* sched_list;            // [n_units] units with work: (unit, q_start, q_len, kv_len)
     int B, H, H_kv, G, T;        // T = tokens per query tile
     int total_q, max_q_len, n_qt;
     int page_size, max_pages, num_pages, rows_per_box;  // rows_per_box = min(page_size, 128)
@@ -91,7 +93,10 @@ constexpr int kPagedThreads = 192;  // TMA warp + MMA warp + one softmax warpgro
 struct PagedPlan {
     int G, T, n_qt, n_splits, split_blocks;
     long long n_units;
-    size_t part_o_bytes, part_ml_bytes, workspace_bytes;  // workspace_bytes == 0: no split
+    size_t list_offset;                  // byte offset of the unit list (after the 256-byte header)
+    size_t part_o_bytes, part_ml_bytes;  // 0 when every unit covers all of its keys
+    size_t part_o_offset, part_ml_offset;
+    size_t workspace_bytes;              // header + list + partials
 };
 PagedPlan paged_plan(int total_q, int max_q_len, int B, int H, int H_kv, int d, int page_size, int max_pages);
 

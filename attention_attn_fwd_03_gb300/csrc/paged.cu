@@ -20,6 +20,10 @@
 // split_blocks KV blocks of 128 keys.  With more than one split the units
 // write unnormalised partials (O_s, m_s, l_s) and a merge kernel combines
 // them with the (m, l, O) merge of the Capstone page, section 2.2 step 4.
+// Request lengths live on the device, so a one-CTA schedule pass first lists
+// the units that have work, longest first; the persistent CTAs then take
+// list entries from an atomic counter (work units differ in size by up to the split length, and
+// dynamic fetching keeps the SMs evenly loaded to the end).
 //
 // Persistent CTAs (one per SM), 192 threads:
 //   warp 0    TMA producer: per unit the Q tile (box: 64 dims x G heads x T
@@ -53,6 +57,9 @@ namespace {
 constexpr float kTau = 8.0f;  // log2 units
 constexpr float kLn2 = 0.69314718055994530942f;
 
+constexpr int kQN = 4;        // unit-queue slots between the producer and the other roles
+constexpr int kSlotInts = 11;  // one decoded unit per slot (see publish_unit)
+
 template <int D>
 struct PCfg {
     static constexpr int NPANEL = D / 64;          // 128-byte panels of the head dim
@@ -61,11 +68,12 @@ struct PCfg {
     static constexpr int NST = D == 128 ? 5 : 8;   // K/V ring stages
     static constexpr uint32_t TM_O = 256;          // S buffers at columns 0 and 128
     static constexpr uint32_t TM_COLS = 512;
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_KV = OFF_Q + TILE_BYTES;
+    static constexpr int OFF_Q = 0;                // two Q tiles
+    static constexpr int OFF_KV = OFF_Q + 2 * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_KV + NST * TILE_BYTES;
-    static constexpr int N_BARS = 2 * NST + 9;
-    static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
+    static constexpr int N_BARS = 2 * NST + 11 + 2 * kQN;
+    static constexpr int OFF_UQ = OFF_BAR + 8 * N_BARS;
+    static constexpr int OFF_MISC = OFF_UQ + 4 * kQN * kSlotInts;
     static constexpr int SMEM_USED = OFF_MISC + 16;
     // more than half an SM's shared memory: one CTA per SM owns all 512 TMEM columns
     static constexpr int SMEM_BYTES = (SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024);
@@ -73,8 +81,8 @@ struct PCfg {
 };
 
 struct PBars {
-    uint64_t* q_full;
-    uint64_t* q_empty;
+    uint64_t* q_full;    // [2], one per Q buffer
+    uint64_t* q_empty;   // [2]
     uint64_t* kv_full;   // [NST]
     uint64_t* kv_empty;  // [NST]
     uint64_t* s_full;    // [2], one per S buffer
@@ -82,6 +90,8 @@ struct PBars {
     uint64_t* o_full;    // one phase per PV product
     uint64_t* o_empty;   // 128 arrivals per unit
     uint64_t* done;
+    uint64_t* uq_full;   // [kQN], the producer published a unit into the slot
+    uint64_t* uq_empty;  // [kQN], 5 arrivals: the MMA issuer and the four softmax warps read it
 };
 
 struct PUnit {
@@ -132,22 +142,58 @@ __device__ __forceinline__ int tile_kv_blocks(const PagedParams& p, int q_len, i
 }
 
 // Unit u: KV head fastest, then request, then query tile (last tiles, the
-// heaviest under the causal mask, first), then split.
-__device__ __forceinline__ PUnit paged_unit(const PagedParams& p, int u) {
-    PUnit g;
+// heaviest under the causal mask, first), then split.  unit_tile fills in
+// the tile and its KV blocks once the request's extent is in g.
+__device__ __forceinline__ void unit_tile(const PagedParams& p, int u, PUnit& g) {
     g.kvh = u % p.H_kv;
     int x = u / p.H_kv;
     g.r = x % p.B;
     x /= p.B;
     const int qt = p.n_qt - 1 - x % p.n_qt;
     g.split = x / p.n_qt;
-    request_extent(p, g.r, g);
     g.t0 = qt * p.T;
     g.nt = min(p.T, g.q_len - g.t0);
     const int nb_all = g.nt > 0 ? tile_kv_blocks(p, g.q_len, g.kv_len, g.t0 + g.nt - 1) : 0;
     g.kb0 = g.split * p.split_blocks;
     g.nb = max(0, min(p.split_blocks, nb_all - g.kb0));
+}
+
+__device__ __forceinline__ PUnit paged_unit(const PagedParams& p, int u) {
+    PUnit g;
+    request_extent(p, (u / p.H_kv) % p.B, g);
+    unit_tile(p, u, g);
     return g;
+}
+
+// Queue slots carry the unit already decoded, so that the MMA issuer and the
+// softmax warps start a unit without global loads on their critical path.
+__device__ __forceinline__ void publish_unit(volatile int* q, int u, const PUnit& g) {
+    q[0] = u;
+    q[1] = g.r;
+    q[2] = g.kvh;
+    q[3] = g.split;
+    q[4] = g.q_start;
+    q[5] = g.q_len;
+    q[6] = g.kv_len;
+    q[7] = g.t0;
+    q[8] = g.nt;
+    q[9] = g.kb0;
+    q[10] = g.nb;
+}
+
+__device__ __forceinline__ int read_unit(const volatile int* q, PUnit& g) {
+    g.r = q[1];
+    g.kvh = q[2];
+    g.split = q[3];
+    g.q_start = q[4];
+    g.q_len = q[5];
+    g.kv_len = q[6];
+    g.t0 = q[7];
+    g.nt = q[8];
+    g.kb0 = q[9];
+    g.nb = q[10];
+    g.bad = false;
+    return q[0];
 }
 
 __device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -162,8 +208,8 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
 // ---------------------------------------------------------------- producer (whole warp)
 
 template <int D>
-__device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag,
-                              int lane) {
+__device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& b, volatile int* uq,
+                              volatile int* abort_flag, int lane) {
     using C = PCfg<D>;
     if (lane == 0) {
         tma_prefetch_map(&p.tm_q);
@@ -171,23 +217,67 @@ __device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& 
         tma_prefetch_map(&p.tm_v);
     }
     const int R = p.rows_per_box;
-    const int LPB = 128 / R;                       // boxes per panel per KV block (1..16)
-    const int oob = p.num_pages * p.page_size;     // first row past the cache: zero fill
-    int kv_idx = 0, qcnt = 0;
+    const int LPB = 128 / R;                    // boxes per panel per KV block (1..16)
+    const int oob = p.num_pages * p.page_size;  // first row past the cache: zero fill
+    int kv_idx = 0, qcnt = 0, pub = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const PUnit g = paged_unit(p, u);
-        if (g.bad && lane == 0) atomicOr(p.status, 1u << kStatusDeviceData);
-        if (g.nb == 0) continue;
-        // the query tile, once the previous unit's last S product released it
+    // the schedule pass listed the units with work; take them in list order
+    // The list built by the schedule pass (entries: unit, q_start, q_len,
+    // kv_len) is taken in order: entry blockIdx.x first (read alongside the
+    // list length; the entry exists since the grid is no larger than the unit
+    // count), then entries gridDim.x, gridDim.x + 1, ... through the fetch
+    // counter.  The next entry is fetched while the current unit's loads are
+    // issued, and no further global load is needed to decode it.
+    griddep_wait();  // the list exists once the schedule pass has completed
+    const int total = p.sched[1];
+    int4 next = make_int4(-1, 0, 0, 0);
+    if (lane == 0) {
+        const int4 e = p.sched_list[blockIdx.x];
+        if ((int)blockIdx.x < total) next = e;
+    }
+    for (;;) {
+        int4 cur;
+        cur.x = __shfl_sync(0xffffffffu, next.x, 0);
+        cur.y = __shfl_sync(0xffffffffu, next.y, 0);
+        cur.z = __shfl_sync(0xffffffffu, next.z, 0);
+        cur.w = __shfl_sync(0xffffffffu, next.w, 0);
+        const int u = cur.x;
+        const bool more = u >= 0;
+        if (more && lane == 0) {
+            const int k = (int)gridDim.x + atomicAdd(p.sched, 1);
+            next = k < total ? p.sched_list[k] : make_int4(-1, 0, 0, 0);
+        }
+        PUnit g{};
+        if (more) {
+            g.q_start = cur.y;
+            g.q_len = cur.z;
+            g.kv_len = cur.w;
+            g.bad = false;
+            unit_tile(p, u, g);
+        }
+        // publish the unit (or the end mark) to the MMA issuer and the softmax warps
         if (lane == 0) {
-            if (qcnt > 0) ok = wait_bar(b.q_empty, (uint32_t)((qcnt - 1) & 1), abort_flag, p.status);
+            const int slot = pub % kQN;
+            if (pub >= kQN) ok = wait_bar(&b.uq_empty[slot], (uint32_t)((pub / kQN - 1) & 1), abort_flag, p.status);
             if (ok) {
-                bar_arrive_expect_tx(b.q_full, p.q_tile_bytes);
+                publish_unit(uq + slot * kSlotInts, more ? u : -1, g);
+                bar_arrive(&b.uq_full[slot]);  // release: the slot's value is visible to the waiters
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok || !more) break;
+        ++pub;
+        if (g.nb == 0) continue;  // only the softmax warps act (zero rows)
+        // the query tile into buffer qcnt & 1, released by the unit two back
+        const int qb = qcnt & 1;
+        if (lane == 0) {
+            if (qcnt >= 2) ok = wait_bar(&b.q_empty[qb], (uint32_t)(((qcnt >> 1) - 1) & 1), abort_flag, p.status);
+            if (ok) {
+                bar_arrive_expect_tx(&b.q_full[qb], p.q_tile_bytes);
 #pragma unroll
                 for (int pn = 0; pn < C::NPANEL; ++pn)
-                    tma_load_3d(smem + C::OFF_Q + pn * C::PANEL_BYTES, &p.tm_q, b.q_full, pn * 64, g.kvh * p.G,
-                                g.q_start + g.t0);
+                    tma_load_3d(smem + C::OFF_Q + qb * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q, &b.q_full[qb],
+                                pn * 64, g.kvh * p.G, g.q_start + g.t0);
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -242,10 +332,12 @@ __device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& 
                 ++kv_idx;
             }
         }
+        if (!ok) break;
     }
     // Drain: every copy this warp started must land before the CTA exits.
     if (lane == 0) {
-        if (qcnt > 0) drain_wait(b.q_full, (uint32_t)((qcnt - 1) & 1), p.status);
+        for (int i = qcnt - 2 > 0 ? qcnt - 2 : 0; i < qcnt; ++i)
+            drain_wait(&b.q_full[i & 1], (uint32_t)((i >> 1) & 1), p.status);
         for (int idx = kv_idx - C::NST > 0 ? kv_idx - C::NST : 0; idx < kv_idx; ++idx)
             drain_wait(&b.kv_full[idx % C::NST], (uint32_t)((idx / C::NST) & 1), p.status);
     }
@@ -255,11 +347,10 @@ __device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& 
 // ---------------------------------------------------------------- MMA issuer (one thread)
 
 template <int D>
-__device__ void mma_role(const PagedParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag,
-                         uint32_t tmem) {
+__device__ void mma_role(const PagedParams& p, uint8_t* smem, const PBars& b, volatile int* uq,
+                         volatile int* abort_flag, uint32_t tmem) {
     using C = PCfg<D>;
     const uint32_t sbase = smem_u32(smem);
-    const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q, 16, 1024);
     const uint32_t kv0 = sbase + C::OFF_KV;
     auto k_desc = [&](int idx) { return sdesc_sw128(kv0 + (uint32_t)((idx % C::NST) * C::TILE_BYTES), 16, 1024); };
     auto v_desc = [&](int idx) {
@@ -271,18 +362,25 @@ __device__ void mma_role(const PagedParams& p, uint8_t* smem, const PBars& b, vo
     const uint32_t d_o = tmem + C::TM_O;
     int kv_base = 0, qcnt = 0, units = 0;
     uint32_t sblk = 0;  // KV blocks processed so far: block sblk uses S buffer sblk & 1
-    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-        const PUnit g = paged_unit(p, u);
+    for (int k = 0;; ++k) {
+        const int slot = k % kQN;
+        if (!wait_bar(&b.uq_full[slot], (uint32_t)((k / kQN) & 1), abort_flag, p.status)) return;
+        PUnit g;
+        const int u = read_unit(uq + slot * kSlotInts, g);
+        bar_arrive(&b.uq_empty[slot]);
+        if (u < 0) break;
         const int nb = g.nb;
         if (nb == 0) continue;
-        if (!wait_bar(b.q_full, (uint32_t)(qcnt & 1), abort_flag, p.status)) return;
+        const int qb = qcnt & 1;
+        if (!wait_bar(&b.q_full[qb], (uint32_t)((qcnt >> 1) & 1), abort_flag, p.status)) return;
         ++qcnt;
+        const uint64_t q_desc = sdesc_sw128(sbase + (uint32_t)(C::OFF_Q + qb * C::TILE_BYTES), 16, 1024);
         if (!wait_full(kv_base)) return;
         tc_fence_after();
         issue_s<D, false>(tmem + (sblk & 1u) * 128u, q_desc, k_desc(kv_base));
         tc_commit(&b.s_full[sblk & 1u]);
         tc_commit(&b.kv_empty[kv_base % C::NST]);
-        if (nb == 1) tc_commit(b.q_empty);
+        if (nb == 1) tc_commit(&b.q_empty[qb]);
         for (int j = 0; j < nb; ++j) {
             const uint32_t sb = sblk + (uint32_t)j;
             const int iV = kv_base + 2 * j + 1, iK1 = kv_base + 2 * j + 2;
@@ -292,7 +390,7 @@ __device__ void mma_role(const PagedParams& p, uint8_t* smem, const PBars& b, vo
                 issue_s<D, false>(tmem + ((sb + 1u) & 1u) * 128u, q_desc, k_desc(iK1));
                 tc_commit(&b.s_full[(sb + 1u) & 1u]);
                 tc_commit(&b.kv_empty[iK1 % C::NST]);
-                if (j + 1 == nb - 1) tc_commit(b.q_empty);
+                if (j + 1 == nb - 1) tc_commit(&b.q_empty[qb]);
             }
             if (!wait_full(iV)) return;
             if (j == 0 && units > 0 && !wait_bar(b.o_empty, (uint32_t)((units - 1) & 1), abort_flag, p.status))
@@ -312,8 +410,8 @@ __device__ void mma_role(const PagedParams& p, uint8_t* smem, const PBars& b, vo
 // ---------------------------------------------------------------- softmax + epilogue
 
 template <int D>
-__device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag,
-                             uint32_t tmem, int wq, int lane) {
+__device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b, volatile int* uq,
+                             volatile int* abort_flag, uint32_t tmem, int wq, int lane) {
     using C = PCfg<D>;
     const int row = wq * 32 + lane;  // tile row == TMEM lane
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
@@ -325,8 +423,15 @@ __device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b
     int kv_base = 0;
     bool ok = true;
 
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const PUnit g = paged_unit(p, u);
+    for (int k = 0; ok; ++k) {
+        const int slot = k % kQN;
+        ok = __all_sync(0xffffffffu, wait_bar(&b.uq_full[slot], (uint32_t)((k / kQN) & 1), abort_flag, p.status));
+        if (!ok) break;
+        PUnit g;
+        const int u = read_unit(uq + slot * kSlotInts, g);
+        __syncwarp();
+        if (lane == 0) bar_arrive(&b.uq_empty[slot]);
+        if (u < 0) break;
         if (g.nt <= 0) continue;
         const bool row_ok = tr < g.nt;
         const int head = g.kvh * p.G + gh;
@@ -465,9 +570,9 @@ __device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b
         reg_after_wait<D>(o);
         tc_fence_before();
         bar_arrive(b.o_empty);
-        if (!row_ok) continue;
         const float m_use = (m == -INFINITY) ? 0.f : m;
         if (p.n_splits == 1) {
+            if (!row_ok) continue;
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
             uint16_t* dst = p.o + grow * D;
 #pragma unroll
@@ -477,7 +582,7 @@ __device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b
                              pack_bf16(__uint_as_float(o[c + 4]) * inv, __uint_as_float(o[c + 5]) * inv),
                              pack_bf16(__uint_as_float(o[c + 6]) * inv, __uint_as_float(o[c + 7]) * inv));
             if (p.lse != nullptr) p.lse[grow] = (l > 0.f) ? (m_use + lg2(l)) * kLn2 : -INFINITY;
-        } else {
+        } else if (row_ok) {
             const size_t rec = grow * (size_t)p.n_splits + (size_t)g.split;
             float* po = p.part_o + rec * D;
 #pragma unroll
@@ -500,25 +605,30 @@ __global__ void __launch_bounds__(kPagedThreads, 1) paged_kernel(const __grid_co
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     PBars b;
     b.q_full = bars;
-    b.q_empty = bars + 1;
-    b.kv_full = bars + 2;
-    b.kv_empty = bars + 2 + C::NST;
-    b.s_full = bars + 2 + 2 * C::NST;
+    b.q_empty = bars + 2;
+    b.kv_full = bars + 4;
+    b.kv_empty = bars + 4 + C::NST;
+    b.s_full = bars + 4 + 2 * C::NST;
     b.p_full = b.s_full + 2;
     b.o_full = b.p_full + 1;
     b.o_empty = b.o_full + 1;
     b.done = b.o_empty + 1;
+    b.uq_full = b.done + 1;
+    b.uq_empty = b.uq_full + kQN;
+    volatile int* uq = reinterpret_cast<volatile int*>(smem + C::OFF_UQ);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     volatile int* skip = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
 
-    if (threadIdx.x == 0) *skip = (*(volatile unsigned*)p.status != 0u) ? 1 : 0;
-    __syncthreads();
-    if (*skip) return;  // an earlier launch gave up: leave the device quiet
-
     if (threadIdx.x == 0) {
-        bar_init(b.q_full, 1);
-        bar_init(b.q_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            bar_init(&b.q_full[i], 1);
+            bar_init(&b.q_empty[i], 1);
+        }
+        for (int i = 0; i < kQN; ++i) {
+            bar_init(&b.uq_full[i], 1);
+            bar_init(&b.uq_empty[i], 5);
+        }
         for (int s = 0; s < C::NST; ++s) {
             bar_init(&b.kv_full[s], 1);
             bar_init(&b.kv_empty[s], 1);
@@ -535,31 +645,37 @@ __global__ void __launch_bounds__(kPagedThreads, 1) paged_kernel(const __grid_co
     if (warp >= 2) {
         // rows of the Q tile that no load writes (G * T < 128, or fewer tokens
         // in the box) must read as zeros, not stale shared memory
-        const uint32_t q0 = smem_u32(smem + C::OFF_Q) + (uint32_t)((threadIdx.x - 64) * (C::TILE_BYTES / 128));
+        const uint32_t q0 = smem_u32(smem + C::OFF_Q) + (uint32_t)((threadIdx.x - 64) * (2 * C::TILE_BYTES / 128));
 #pragma unroll
-        for (int c = 0; c < C::TILE_BYTES / 128; c += 16) st_shared_zero16(q0 + (uint32_t)c);
+        for (int c = 0; c < 2 * C::TILE_BYTES / 128; c += 16) st_shared_zero16(q0 + (uint32_t)c);
         fence_async_smem();
     }
     if (warp == 0) {
         tmem_alloc(tmem_holder, C::TM_COLS);
         tmem_relinquish();
     }
+    griddep_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid
+    if (threadIdx.x == 0) *skip = (*(volatile unsigned*)p.status != 0u) ? 1 : 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    if (*skip) {  // an earlier launch gave up
+        if (warp == 0) tmem_dealloc(tmem, C::TM_COLS);
+        return;
+    }
 
     if (warp >= 2) {
-        softmax_role<D>(p, smem, b, abort_flag, tmem, warp & 3, lane);
+        softmax_role<D>(p, smem, b, uq, abort_flag, tmem, warp & 3, lane);
     } else if (warp == 1) {
         if (lane == 0) {
-            mma_role<D>(p, smem, b, abort_flag, tmem);
+            mma_role<D>(p, smem, b, uq, abort_flag, tmem);
             tc_commit(b.done);  // every issued MMA finishes before tensor memory is released
             drain_wait(b.done, 0, p.status);
         }
         __syncwarp();
     } else {
-        producer_role<D>(p, smem, b, abort_flag, lane);
+        producer_role<D>(p, smem, b, uq, abort_flag, lane);
     }
 
     tc_fence_before();
@@ -570,12 +686,108 @@ __global__ void __launch_bounds__(kPagedThreads, 1) paged_kernel(const __grid_co
     }
 }
 
+// Schedule pass (one CTA): the list of units that have work (KV blocks to
+// process, or rows to zero when nothing is visible), each entry the unit and
+// its request's extent (q_start, q_len, kv_len); its length in sched[1]; the
+// fetch counter sched[0] reset to 0.  The list is ordered by work, longest
+// first (units with at least kBuckets - 1 blocks share the first bucket), so
+// the last units the persistent CTAs take are the shortest.  The H_kv units
+// of one (split, tile, request) group have the same work and are listed
+// together.  Requests whose offsets or length are out of range are reported
+// here, and their clamped extent is what the list carries.
+constexpr int kBuckets = 64;
+constexpr int kCachedReqs = 2048;
+
+__global__ void __launch_bounds__(1024) paged_schedule_kernel(const PagedParams p) {
+    __shared__ int s_qstart[kCachedReqs], s_qlen[kCachedReqs], s_kvlen[kCachedReqs];
+    __shared__ int s_bucket[kBuckets];
+    griddep_launch_dependents();  // the paged kernel may start its prologue now
+    const int t = threadIdx.x, lane = t & 31;
+    const bool cached = p.B <= kCachedReqs;
+    bool bad = false;
+    for (int r = t; r < p.B; r += 1024) {
+        PUnit g;
+        request_extent(p, r, g);
+        bad |= g.bad;
+        if (cached) {
+            s_qstart[r] = g.q_start;
+            s_qlen[r] = g.q_len;
+            s_kvlen[r] = g.kv_len;
+        }
+    }
+    if (bad) atomicOr(p.status, 1u << kStatusDeviceData);
+    if (t < kBuckets) s_bucket[t] = 0;
+    __syncthreads();
+    // group gi -> its first unit gi * H_kv, the request's extent, and its
+    // work: KV blocks (0 for a unit that only zeroes rows), -1 for none
+    auto group = [&](int gi, PUnit& g) {
+        const int r = gi % p.B;
+        if (cached) {
+            g.q_start = s_qstart[r];
+            g.q_len = s_qlen[r];
+            g.kv_len = s_kvlen[r];
+        } else {
+            request_extent(p, r, g);
+        }
+        unit_tile(p, gi * p.H_kv, g);
+        if (g.nb > 0) return g.nb;
+        return (p.n_splits == 1 && g.nt > 0) ? 0 : -1;
+    };
+    auto bucket = [](int w) { return w >= kBuckets - 1 ? 0 : kBuckets - 1 - w; };  // longest first
+    // Lanes of a warp that hit the same bucket add to it once, through their
+    // leader; the returned base plus the lane's rank among them (times H_kv
+    // entries per lane) is its place.
+    auto reserve = [&](int bk, bool active) {
+        const unsigned act = __ballot_sync(0xffffffffu, active);
+        const unsigned peers = __match_any_sync(0xffffffffu, active ? bk : -1) & act;
+        const int leader = __ffs(peers) - 1;
+        int base = 0;
+        if (active && lane == leader) base = atomicAdd(&s_bucket[bk], __popc(peers) * p.H_kv);
+        base = __shfl_sync(0xffffffffu, base, leader < 0 ? 0 : leader);
+        return base + __popc(peers & ((1u << lane) - 1u)) * p.H_kv;
+    };
+    const int n_groups = p.n_units / p.H_kv;
+    const int n_pad = (n_groups + 1023) / 1024 * 1024;  // every lane of a warp runs every round
+    for (int gi = t; gi < n_pad; gi += 1024) {
+        PUnit g;
+        const int w = gi < n_groups ? group(gi, g) : -1;
+        reserve(w >= 0 ? bucket(w) : 0, w >= 0);
+    }
+
+    __syncthreads();
+    if (t < 32) {  // exclusive scan of the 64 bucket counts (two per lane)
+        const int a = s_bucket[2 * t], b = s_bucket[2 * t + 1];
+        int x = a + b;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (t >= o) x += y;
+        }
+        const int excl = x - a - b;
+        s_bucket[2 * t] = excl;
+        s_bucket[2 * t + 1] = excl + a;
+        if (t == 31) p.sched[1] = x;
+    }
+    __syncthreads();
+    for (int gi = t; gi < n_pad; gi += 1024) {
+        PUnit g;
+        const int w = gi < n_groups ? group(gi, g) : -1;
+        const int pos = reserve(w >= 0 ? bucket(w) : 0, w >= 0);
+        if (w >= 0)
+            for (int h = 0; h < p.H_kv; ++h)
+                p.sched_list[pos + h] = make_int4(gi * p.H_kv + h, g.q_start, g.q_len, g.kv_len);
+    }
+    if (t == 0) p.sched[0] = 0;
+}
+
 // One warp per output row (query token, query head): combine the row's
 // splits with the (m, l, O) merge, m = max_s m_s, l = sum_s l_s 2^(m_s - m),
 // O = sum_s 2^(m_s - m) O_s / l, and write O (bf16) and the LSE.
 template <int D>
-__global__ void __launch_bounds__(256) paged_merge_kernel(const PagedParams p) {
+__global__ void __launch_bounds__(512) paged_merge_kernel(const PagedParams p) {
     constexpr int PER = D / 32;
+    static_assert(PER == 4 || PER == 2, "head dim");
+    griddep_wait();  // launched early: the partials are complete past this point
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (gw >= (long long)p.total_q * p.H) return;
@@ -601,35 +813,63 @@ __global__ void __launch_bounds__(256) paged_merge_kernel(const PagedParams p) {
     const int ns = (nb + p.split_blocks - 1) / p.split_blocks;
     const size_t rec0 = (size_t)gw * p.n_splits;
 
+    // lane s holds split s's (m, l) for s < 32 (more splits: further rounds)
     float m = -INFINITY;
     for (int s = lane; s < ns; s += 32) m = fmaxf(m, p.part_ml[(rec0 + s) * 2]);
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float l = 0.f;
-    if (m != -INFINITY) {
-        for (int s = lane; s < ns; s += 32) {
-            const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (rec0 + s) * 2);
-            l += ml.y * ex2(ml.x - m);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-
     float acc[PER];
 #pragma unroll
     for (int c = 0; c < PER; ++c) acc[c] = 0.f;
     if (m != -INFINITY) {
-        for (int s = 0; s < ns; ++s) {
-            const float w = ex2(p.part_ml[(rec0 + s) * 2] - m);
-            const float* src = p.part_o + (rec0 + s) * D + lane * PER;
+        for (int s0 = 0; s0 < ns; s0 += 32) {
+            float w_mine = 0.f;  // weight 2^(m_s - m) of this lane's split
+            if (s0 + lane < ns) {
+                const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (rec0 + s0 + lane) * 2);
+                w_mine = ex2(ml.x - m);
+                l += ml.y * w_mine;
+            }
+            const int cnt = min(32, ns - s0);
+            // lane owns PER consecutive dims of O: one 16-byte (d = 128) or
+            // 8-byte (d = 64) load per split, eight loads in flight
+            for (int s = 0; s < cnt; s += 8) {
+                float w[8];
+                float v[8][PER];
 #pragma unroll
-            for (int c = 0; c < PER; ++c) acc[c] = fmaf(w, src[c], acc[c]);
+                for (int i = 0; i < 8; ++i) {
+                    w[i] = __shfl_sync(0xffffffffu, w_mine, (s + i) & 31);
+                    const bool in = s + i < cnt;
+                    const float* src = p.part_o + (rec0 + s0 + s + (in ? i : 0)) * D + lane * PER;
+                    if (PER == 4) {
+                        const float4 x = in ? *reinterpret_cast<const float4*>(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+                        v[i][0] = x.x;
+                        v[i][1] = x.y;
+                        v[i][PER > 2 ? 2 : 0] = x.z;
+                        v[i][PER > 3 ? 3 : 0] = x.w;
+                    } else {
+                        const float2 x = in ? *reinterpret_cast<const float2*>(src) : make_float2(0.f, 0.f);
+                        v[i][0] = x.x;
+                        v[i][1] = x.y;
+                    }
+                    if (!in) w[i] = 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int c = 0; c < PER; ++c) acc[c] = fmaf(w[i], v[i][c], acc[c]);
+            }
         }
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     const float inv = (l > 0.f) ? 1.f / l : 0.f;
     uint16_t* dst = p.o + (size_t)gw * D + lane * PER;
-#pragma unroll
-    for (int c = 0; c < PER; c += 2) *reinterpret_cast<uint32_t*>(dst + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
+    if (PER == 4)
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv),
+                                                    pack_bf16(acc[2] * inv, acc[3] * inv));
+    else
+        *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
     if (lane == 0 && p.lse != nullptr) p.lse[gw] = (l > 0.f) ? (m + lg2(l)) * kLn2 : -INFINITY;
 }
 
@@ -639,12 +879,30 @@ cudaError_t launch_d(const PagedParams& p, int grid, cudaStream_t stream) {
     cudaError_t e =
         cudaFuncSetAttribute(paged_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    paged_kernel<D><<<grid, kPagedThreads, C::SMEM_BYTES, stream>>>(p);
+    paged_schedule_kernel<<<1, 1024, 0, stream>>>(p);
     e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // programmatic dependent launches: the paged kernel's prologue overlaps
+    // the schedule pass and its producer waits for the pass (griddepcontrol.wait)
+    // before reading the list; the merge kernel is scheduled early and waits
+    // for the paged kernel to complete
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kPagedThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, paged_kernel<D>, p);
     if (e != cudaSuccess || p.n_splits == 1) return e;
     const long long warps = (long long)p.total_q * p.H;
-    paged_merge_kernel<D><<<(unsigned)((warps + 7) / 8), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)((warps + 15) / 16));
+    cfg.blockDim = dim3(512);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, paged_merge_kernel<D>, p);
 }
 
 }  // namespace
@@ -673,11 +931,17 @@ PagedPlan paged_plan(int total_q, int max_q_len, int B, int H, int H_kv, int d, 
     pl.split_blocks = (int)sb;
     pl.n_splits = (int)((kv_blocks + sb - 1) / sb);
     pl.n_units = base * pl.n_splits;
+    // header (fetch counter, list length), the unit list, then the partials
+    pl.list_offset = 256;
+    pl.workspace_bytes = 256 + ((size_t)pl.n_units * 16 + 255) / 256 * 256;
     if (pl.n_splits > 1) {
         const size_t recs = (size_t)total_q * H * pl.n_splits;
         pl.part_o_bytes = recs * d * sizeof(float);
         pl.part_ml_bytes = recs * 2 * sizeof(float);
-        pl.workspace_bytes = (pl.part_o_bytes + 255) / 256 * 256 + pl.part_ml_bytes;
+        pl.part_o_offset = pl.workspace_bytes;
+        pl.workspace_bytes += (pl.part_o_bytes + 255) / 256 * 256;
+        pl.part_ml_offset = pl.workspace_bytes;
+        pl.workspace_bytes += pl.part_ml_bytes;
     }
     return pl;
 }

@@ -53,7 +53,6 @@ constexpr float kLn2 = 0.69314718055994530942f;
 template <int D, bool FP8>
 struct Cfg {
     static constexpr int EB = FP8 ? 1 : 2;         // bytes per input element
-    static constexpr int BN = 128;                 // keys per KV block
     static constexpr int PANEL = 128 / EB;         // elements in one 128-byte row panel
     static constexpr int NPANEL = D / PANEL;       // panels per row
     static constexpr int PANEL_BYTES = 128 * 128;  // 128 rows x 128 B

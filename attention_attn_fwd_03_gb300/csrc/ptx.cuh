@@ -98,6 +98,15 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
     }
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start while its predecessor runs; griddep_wait blocks
+// until the predecessor grid has completed and its writes are visible, and
+// griddep_launch_dependents lets the next such grid be scheduled early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Wait that ignores the abort flag (used only to drain in-flight async work
 // before the CTA releases its shared and tensor memory); bounded in time.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, unsigned* status) {

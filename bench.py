@@ -10,8 +10,11 @@ write) before every timed step, outside the timed events.
 
 Also reported in the same JSON line (timed the same way, not part of
 `value`): the long causal prefill (1x32x32768, d=128), FP8 prefill
-(2x16x8192, d=128) and paged decode (64 requests, H=32, d=128, 64-token
-pages) -- the latter as HBM GB/s of algorithmic bytes.
+(2x16x8192, d=128), paged decode (64 requests, H=32, d=128, 64-token
+pages), the same decode with 32 query heads over 8 KV heads on the tensor
+cores -- both as HBM GB/s of algorithmic bytes -- and causal prefill chunks
+over a paged cache (8 requests x 2048 new tokens after 6144 cached, 32 query
+heads over 8 KV heads) as TFLOPS of exactly counted visible pairs.
 
 `--impl reference` times the float64 CPU oracle (the only reference this
 method has) on a bounded row sample of the same workload.
@@ -408,6 +411,54 @@ def run_secondary(torch, attn, inputs, dev, flush, peaks, rank):
         "tokens": total_tokens}
     del p, o, l, ws
     torch.cuda.empty_cache()
+    # grouped-query paged decode on the tensor cores: 32 query heads over 8 KV heads
+    p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
+                        len_hi=8192, seed=rank, device=dev, H_kv=8)
+    o = torch.empty_like(p["q"])
+    l = torch.empty((64, 32), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, attn.attn_paged_fwd_workspace_size(64, 64, 1, 32, 8, 128, 64, 128)),
+                     dtype=torch.uint8, device=dev)
+
+    def gqa():
+        attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], out=o, lse=l,
+                       workspace=ws)
+    gqa()
+    ms = timed_launches(torch, gqa, reps, flush)
+    attn.device_status()
+    total_tokens = int(p["seq_lens"].sum().item())
+    n_pages = int(((p["seq_lens"].long() + 63) // 64).sum().item())
+    alg_bytes = total_tokens * 8 * 128 * 2 * 2 + 2 * (64 * 32 * 128 * 2) + 64 * 32 * 4 + n_pages * 4 + 64 * 4
+    gbs = alg_bytes / (statistics.mean(ms) * 1e-3) / 1e9
+    out["gqa_paged_decode_64req_H32_Hkv8_d128_p64"] = {
+        "GBps": round(gbs, 1), "ms": round(statistics.mean(ms), 4), "algorithmic_bytes": alg_bytes,
+        "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4), "frac_of_8TBps": round(gbs / 8000.0, 4),
+        "tokens": total_tokens}
+    del p, o, l, ws
+    torch.cuda.empty_cache()
+    # prefill chunks over a paged cache: 8 requests, 2048 new tokens after a 6144-token prefix, causal
+    p = inputs.paged_chunks(B=8, H=32, H_kv=8, d=128, page_size=64, max_pages=128, num_pages=1024,
+                            q_lo=2048, q_hi=2048, ctx_lo=6144, ctx_hi=6144, seed=rank, device=dev)
+    o = torch.empty_like(p["q"])
+    l = torch.empty((p["q"].shape[0], 32), dtype=torch.float32, device=dev)
+    wsb = attn.attn_paged_fwd_workspace_size(8, p["q"].shape[0], 2048, 32, 8, 128, 64, 128)
+    ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=dev)
+
+    def chunks():
+        attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"],
+                       cu_seqlens_q=p["cu_seqlens_q"], max_q_len=2048, causal=True, out=o, lse=l, workspace=ws)
+    chunks()
+    ms = timed_launches(torch, chunks, reps, flush)
+    attn.device_status()
+    # exact visible (query, key) pairs: query i of a request sees 6144 + i + 1 keys
+    pairs = 8 * sum(6144 + i + 1 for i in range(2048))
+    f = 4.0 * pairs * 32 * 128
+    tf = f / (statistics.mean(ms) * 1e-3) / 1e12
+    out["paged_prefill_chunks_8x2048_over_6144_H32_Hkv8_d128_causal"] = {
+        "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
+        "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4),
+        "flops_note": "4 * d * H * visible (query, key) pairs, counted exactly"}
+    del p, o, l, ws
+    torch.cuda.empty_cache()
     return out
 
 
@@ -517,6 +568,19 @@ def run_profile_case(args):
         p = inputs.paged_kv(B=8, H=32, d=128, page_size=64, max_pages=128, num_pages=1024, len_lo=512,
                             len_hi=8192, seed=0, device=dev)
         fns = [lambda: attn.paged_decode(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"])]
+    elif case == "gqa_decode_small":
+        p = inputs.paged_kv(B=16, H=32, d=128, page_size=64, max_pages=128, num_pages=2048, len_lo=512,
+                            len_hi=8192, seed=0, device=dev, H_kv=8)
+        fns = [lambda: attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"])]
+    elif case == "gqa_decode":
+        p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
+                            len_hi=8192, seed=0, device=dev, H_kv=8)
+        fns = [lambda: attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"])]
+    elif case == "chunks_small":
+        p = inputs.paged_chunks(B=2, H=32, H_kv=8, d=128, page_size=64, max_pages=128, num_pages=256,
+                                q_lo=2048, q_hi=2048, ctx_lo=6144, ctx_hi=6144, seed=0, device=dev)
+        fns = [lambda: attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"],
+                                      cu_seqlens_q=p["cu_seqlens_q"], max_q_len=2048, causal=True)]
     else:
         raise SystemExit("unknown --profile-case %s" % case)
     for _ in range(args.warmup):
@@ -544,7 +608,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["step", "long_small", "fp8", "decode_small"], default=None,
+    ap.add_argument("--profile-case", choices=["step", "long_small", "fp8", "decode_small", "gqa_decode_small",
+                                               "gqa_decode", "chunks_small"], default=None,
                     help="run one small workload for an ncu capture instead of the benchmark")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps

@@ -141,9 +141,11 @@ attn_status_t attn_paged_decode_noalloc(const void* q, const void* k_cache, cons
                                         int B, int H, int d, int page_size, int max_pages_per_seq,
                                         int num_pages, float scale, void* o, float* lse, void* stream);
 
-/* Bytes of device workspace attn_paged_fwd needs for these sizes; 0 when no
- * workspace is needed (every unit covers all of its keys) or the sizes are
- * invalid.  The workspace holds per-split partials (unnormalised O, m, l). */
+/* Bytes of device workspace attn_paged_fwd needs for these sizes (0 on
+ * invalid sizes): a work list (which work units have keys to process, built
+ * by each call on `stream`, and the counter its CTAs take entries with) and,
+ * when a request's keys are split over several CTAs, the per-split partials
+ * (unnormalised O, m, l). */
 size_t attn_paged_fwd_workspace_size(int B, int total_q, int max_q_len, int H, int H_kv, int d, int page_size,
                                      int max_pages_per_seq);
 
@@ -169,8 +171,9 @@ size_t attn_paged_fwd_workspace_size(int B, int total_q, int max_q_len, int H, i
  *   causal: 1 = query at position P sees keys t <= P (the bottom-right
  *     aligned lower triangle of attn_fwd); 0 = every query sees all keys
  *   o: bf16 [total_q, H, d]; lse: fp32 [total_q, H] or NULL
- *   workspace: at least attn_paged_fwd_workspace_size(...) bytes (may be NULL
- *     when that is 0), caller-owned, contents need no initialisation
+ *   workspace: at least attn_paged_fwd_workspace_size(...) bytes,
+ *     caller-owned, 16-byte aligned, contents need no initialisation; calls
+ *     that may overlap on the GPU need distinct workspaces
  *   d in {64, 128}; page_size a power of two in [8, 1024]; H % H_kv == 0 and
  *   H / H_kv <= 128.
  * A query with no visible key gets O = 0 and lse = -inf.

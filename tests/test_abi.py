@@ -122,8 +122,8 @@ def test_paged_fwd_workspace_size_query(L):
     # one token per request over 8192-key caches: runs of 8 KV blocks, 8 splits
     ws = attn.attn_paged_fwd_workspace_size(64, 64, 1, 32, 8, 128, 64, 128)
     assert ws >= 64 * 32 * 8 * 130 * 4
-    # everything fits one split: no workspace
-    assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 2, 128, 64, 16) == 0
+    # everything fits one split: only the work list (8 entries of 16 bytes, rounded to 256) and its header
+    assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 2, 128, 64, 16) == 512
     assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 3, 128, 64, 16) == 0  # H % H_kv != 0
     assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 2, 128, 48, 16) == 0  # page size not a power of two
     assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 512, 2, 128, 64, 16) == 0  # 256 heads per group
@@ -142,6 +142,7 @@ def test_paged_fwd_validation(L):
     assert attn.attn_paged_fwd(**dict(base, q=FAKE + 8)) == attn.ATTN_ERR_INVALID_ARG
     assert attn.attn_paged_fwd(**dict(base, num_pages=0)) == attn.ATTN_ERR_INVALID_ARG
     assert attn.attn_paged_fwd(**dict(base, seq_lens=None)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_paged_fwd(**base) == attn.ATTN_ERR_WORKSPACE  # the work list is always needed
     long = dict(base, max_pages_per_seq=128, num_pages=1024)
     ws = attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 2, 128, 64, 128)
     assert ws > 0
