@@ -8,10 +8,11 @@ Two levels:
   * ``attn_fwd``, ``attn_fwd_fp8``, ``attn_paged_decode``,
     ``attn_paged_decode_workspace_size``, ``attn_paged_decode_noalloc``,
     ``attn_paged_fwd``, ``attn_paged_fwd_workspace_size``,
+    ``attn_varlen_fwd``, ``attn_varlen_fwd_workspace_size``,
     ``attn_device_status``, ``attn_status_string``: the C entry points, same
     names and argument order, taking raw device pointers (ints) and a stream
     handle (int).
-  * ``fwd``, ``fwd_fp8``, ``paged_decode``, ``paged_fwd``: take torch CUDA
+  * ``fwd``, ``fwd_fp8``, ``paged_decode``, ``paged_fwd``, ``varlen_fwd``: take torch CUDA
     tensors, allocate
     outputs with torch when none are given, call the C entry point on the
     current stream and raise ``AttnError`` on a non-zero status.
@@ -79,6 +80,10 @@ def lib():
             L.attn_paged_fwd.restype = i
             L.attn_paged_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, sz,
                                          vp]
+            L.attn_varlen_fwd_workspace_size.restype = sz
+            L.attn_varlen_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.attn_varlen_fwd.restype = i
+            L.attn_varlen_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, sz, vp]
             L.attn_device_status.restype = i
             L.attn_device_status.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -127,6 +132,16 @@ def attn_paged_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, B, 
     return lib().attn_paged_fwd(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, B, total_q, max_q_len,
                                 H, H_kv, d, page_size, max_pages_per_seq, num_pages, scale, causal, o, lse,
                                 workspace, workspace_bytes, stream)
+
+
+def attn_varlen_fwd_workspace_size(B, total_q, max_q_len, max_k_len, H, H_kv, d):
+    return lib().attn_varlen_fwd_workspace_size(B, total_q, max_q_len, max_k_len, H, H_kv, d)
+
+
+def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, B, total_q, total_k, max_q_len, max_k_len, H, H_kv, d,
+                    scale, causal, o, lse, workspace, workspace_bytes, stream):
+    return lib().attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, B, total_q, total_k, max_q_len, max_k_len, H,
+                                 H_kv, d, scale, causal, o, lse, workspace, workspace_bytes, stream)
 
 
 def attn_device_status(stream):
@@ -295,6 +310,50 @@ def paged_fwd(q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q=None, max
                         out.data_ptr(), lse.data_ptr() if lse is not None else None, workspace.data_ptr(),
                         workspace.numel(), _stream(stream))
     _raise(st, "attn_paged_fwd")
+    return out, lse
+
+
+def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q_len=None, max_k_len=None, causal=False, scale=None,
+               out=None, lse=None, workspace=None, return_lse=True, stream=None):
+    """Variable-length batch prefill with grouped KV heads.
+
+    q bf16 [total_q, H, d]; k, v bf16 [total_k, H_kv, d]; cu_seqlens_q,
+    cu_seqlens_k int32 [B+1] row offsets.  max_q_len / max_k_len are the
+    largest per-request counts (read from the offsets, with a device-to-host
+    copy, when not given).  Returns (o bf16 like q, lse fp32 [total_q, H]).
+    """
+    torch = _torch()
+    total_q, H, d = q.shape
+    total_k, H_kv = k.shape[0], k.shape[1]
+    B = cu_seqlens_q.shape[0] - 1
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16, (total_k, H_kv, d))
+    _check(v, "v", torch.bfloat16, (total_k, H_kv, d))
+    _check(cu_seqlens_q, "cu_seqlens_q", torch.int32, (B + 1,))
+    _check(cu_seqlens_k, "cu_seqlens_k", torch.int32, (B + 1,))
+    if max_q_len is None:
+        max_q_len = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item()) if B else 0
+    if max_k_len is None:
+        max_k_len = int((cu_seqlens_k[1:] - cu_seqlens_k[:-1]).max().item()) if B else 0
+    if out is None:
+        out = torch.empty_like(q)
+    _check(out, "out", torch.bfloat16, (total_q, H, d))
+    if lse is None and return_lse:
+        lse = torch.empty((total_q, H), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check(lse, "lse", torch.float32, (total_q, H))
+    ws_bytes = attn_varlen_fwd_workspace_size(B, total_q, max_q_len, max_k_len, H, H_kv, d)
+    if ws_bytes == 0:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "attn_varlen_fwd_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    st = attn_varlen_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(),
+                         B, total_q, total_k, max_q_len, max_k_len, H, H_kv, d, sc, int(bool(causal)), out.data_ptr(),
+                         lse.data_ptr() if lse is not None else None, workspace.data_ptr(), workspace.numel(),
+                         _stream(stream))
+    _raise(st, "attn_varlen_fwd")
     return out, lse
 
 

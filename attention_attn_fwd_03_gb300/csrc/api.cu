@@ -300,6 +300,77 @@ attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_c
     p.max_pages = max_pages_per_seq;
     p.num_pages = num_pages;
     p.rows_per_box = R;
+    p.kv_rows = (int)slots;
+    p.causal = causal;
+    p.n_splits = pl.n_splits;
+    p.split_blocks = pl.split_blocks;
+    p.n_units = (int)pl.n_units;
+    p.q_tile_bytes = (uint32_t)(d / 64) * (uint32_t)(pl.G * pl.T) * 128u;
+    p.c_scale = scale * 1.4426950408889634f;
+    const int grid = pl.n_units < ds->sm_count ? (int)pl.n_units : ds->sm_count;  // persistent: one CTA per SM
+    return from_cuda(launch_paged(d, p, grid, static_cast<cudaStream_t>(stream)));
+}
+
+size_t attn_varlen_fwd_workspace_size(int B, int total_q, int max_q_len, int max_k_len, int H, int H_kv, int d) {
+    if (max_k_len < 1) return 0;
+    const int max_blocks = (int)(((long long)max_k_len + 127) / 128);
+    if (paged_sizes_ok(B, total_q, max_q_len, H, H_kv, d, 128, max_blocks) != ATTN_OK) return 0;
+    return paged_plan(total_q, max_q_len, B, H, H_kv, d, 128, max_blocks).workspace_bytes;
+}
+
+attn_status_t attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_k, int B, int total_q, int total_k, int max_q_len,
+                              int max_k_len, int H, int H_kv, int d, float scale, int causal, void* o, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !cu_seqlens_q || !cu_seqlens_k || !o) return ATTN_ERR_INVALID_ARG;
+    if (total_k < 1 || max_k_len < 1 || max_k_len > total_k) return ATTN_ERR_INVALID_ARG;
+    const int max_blocks = (int)(((long long)max_k_len + 127) / 128);
+    attn_status_t st = paged_sizes_ok(B, total_q, max_q_len, H, H_kv, d, 128, max_blocks);
+    if (st != ATTN_OK) return st;
+    if ((long long)total_k + 128 > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+    auto a4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
+    if (!a4(cu_seqlens_q) || !a4(cu_seqlens_k) || (lse && !a4(lse))) return ATTN_ERR_INVALID_ARG;
+    const PagedPlan pl = paged_plan(total_q, max_q_len, B, H, H_kv, d, 128, max_blocks);
+    if (pl.n_units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < pl.workspace_bytes || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+
+    DeviceState* ds = nullptr;
+    st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+
+    PagedParams p;
+    std::memset(&p, 0, sizeof p);
+    if (!make_paged_map(&p.tm_q, q, d, H, total_q, pl.G, pl.T) || !make_paged_map(&p.tm_k, k, d, H_kv, total_k, 1, 128) ||
+        !make_paged_map(&p.tm_v, v, d, H_kv, total_k, 1, 128))
+        return ATTN_ERR_CUDA;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.o = static_cast<uint16_t*>(o);
+    p.lse = lse;
+    p.sched = static_cast<int*>(workspace);
+    char* ws = static_cast<char*>(workspace);
+    p.sched_list = reinterpret_cast<int4*>(ws + pl.list_offset);
+    if (pl.n_splits > 1) {
+        p.part_o = reinterpret_cast<float*>(ws + pl.part_o_offset);
+        p.part_ml = reinterpret_cast<float*>(ws + pl.part_ml_offset);
+    }
+    p.status = ds->status;
+    p.B = B;
+    p.H = H;
+    p.H_kv = H_kv;
+    p.G = pl.G;
+    p.T = pl.T;
+    p.total_q = total_q;
+    p.max_q_len = max_q_len;
+    p.n_qt = pl.n_qt;
+    p.page_size = 128;
+    p.max_pages = max_blocks;
+    p.num_pages = 0;
+    p.rows_per_box = 128;
+    p.kv_rows = total_k;
     p.causal = causal;
     p.n_splits = pl.n_splits;
     p.split_blocks = pl.split_blocks;

@@ -69,7 +69,8 @@ struct PagedParams {
     CUtensorMap tm_v;
     const int32_t* block_table;  // [B, max_pages]
     const int32_t* cu_q;         // [B + 1] token offsets, or nullptr: one token per request
-    const int32_t* seq_lens;     // [B] keys per request
+    const int32_t* seq_lens;     // [B] keys per request (paged)
+    const int32_t* cu_k;         // [B + 1] key offsets into contiguous K/V, or nullptr: paged
     uint16_t* o;                 // bf16 [total_q, H, d]
     float* lse;                  // [total_q, H] or nullptr
     float* part_o;               // [total_q * H, n_splits, d] unnormalised partial O (n_splits > 1)
@@ -80,6 +81,7 @@ struct PagedParams {
     int B, H, H_kv, G, T;        // T = tokens per query tile
     int total_q, max_q_len, n_qt;
     int page_size, max_pages, num_pages, rows_per_box;  // rows_per_box = min(page_size, 128)
+    int kv_rows;                 // rows of the K/V tensor maps (slots, or total_k): past them reads zeros
     int causal;
     int n_splits, split_blocks;  // split s covers KV blocks [s, s + 1) * split_blocks
     int n_units;                 // B * H_kv * n_qt * n_splits

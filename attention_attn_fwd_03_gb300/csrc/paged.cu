@@ -1,5 +1,7 @@
 // paged.cu -- exact attention over a paged KV cache on the tensor cores:
-// grouped-query decode and prefill chunks appended to cached prefixes.
+// grouped-query decode and prefill chunks appended to cached prefixes; the
+// same kernel also takes contiguous ragged K/V (variable-length batch
+// prefill, key t of request r at row cu_k[r] + t).
 //
 // The cache is the block-table layout of "FlashAttention V3 实战: Hopper 架构下
 // 的 Paged KV Cache 协同优化", section 3.2 (fixed-size pages named by a
@@ -121,7 +123,16 @@ __device__ __forceinline__ void request_extent(const PagedParams& p, int r, PUni
         g.q_len = 1;
     }
     const int cap = p.max_pages * p.page_size;
-    g.kv_len = __ldg(p.seq_lens + r);
+    if (p.cu_k != nullptr) {  // contiguous keys: rows cu_k[r] .. cu_k[r+1] - 1
+        const int a = __ldg(p.cu_k + r), b = __ldg(p.cu_k + r + 1);
+        g.kv_len = b - a;
+        if (a < 0 || b < a || b > p.kv_rows) {
+            g.bad = true;
+            g.kv_len = 0;
+        }
+    } else {
+        g.kv_len = __ldg(p.seq_lens + r);
+    }
     if (g.kv_len < 0 || g.kv_len > cap) {
         g.bad = true;
         g.kv_len = g.kv_len < 0 ? 0 : cap;
@@ -218,7 +229,7 @@ __device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& 
     }
     const int R = p.rows_per_box;
     const int LPB = 128 / R;                    // boxes per panel per KV block (1..16)
-    const int oob = p.num_pages * p.page_size;  // first row past the cache: zero fill
+    const int oob = p.kv_rows;  // first row past the K/V tensor: zero fill
     int kv_idx = 0, qcnt = 0, pub = 0;
     bool ok = true;
     // the schedule pass listed the units with work; take them in list order
@@ -283,9 +294,11 @@ __device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& 
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         ++qcnt;  // counts issued loads only: the drain below waits for each
-        // K and V blocks; lane i holds the cache row of box (batch * 32 + i)
+        // K and V blocks; lane i holds the cache row of box (batch * 32 + i):
+        // through the block table, or cu_k[r] + key for contiguous keys
         const long long key0 = (long long)g.kb0 * 128;
         const int n_boxes = g.nb * LPB;
+        const int kst = p.cu_k != nullptr ? min(max(__ldg(p.cu_k + g.r), 0), oob) : 0;
         int my_row = oob;
         for (int j = 0; ok && j < g.nb; ++j) {
             const int box0 = j * LPB;
@@ -295,12 +308,16 @@ __device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& 
                 if (bi < n_boxes) {
                     const long long key = key0 + (long long)bi * R;
                     if (key < g.kv_len) {
-                        const int pg = (int)(key / p.page_size);
-                        const int id = __ldg(p.block_table + (size_t)g.r * p.max_pages + pg);
-                        if (id >= 0 && id < p.num_pages)
-                            row = id * p.page_size + (int)(key % p.page_size);
-                        else
-                            atomicOr(p.status, 1u << kStatusDeviceData);
+                        if (p.cu_k != nullptr) {
+                            row = kst + (int)key;
+                        } else {
+                            const int pg = (int)(key / p.page_size);
+                            const int id = __ldg(p.block_table + (size_t)g.r * p.max_pages + pg);
+                            if (id >= 0 && id < p.num_pages)
+                                row = id * p.page_size + (int)(key % p.page_size);
+                            else
+                                atomicOr(p.status, 1u << kStatusDeviceData);
+                        }
                     }
                 }
                 my_row = row;

@@ -27,6 +27,8 @@ discuss -- prefill over BHSD tensors and one-token decode over a paged cache):
   prefix lengths (uniform in [ctx_lo, ctx_hi]), then q [total_q, H, d]
   token-major; seq_len = prefix + q_len keys per request, pages assigned in
   request order from the permutation; caches as for paged decode.
+* variable-length batch: per-request q_len, then prefixes, then packed q,
+  k, v (see varlen_qkv).
 """
 import math
 
@@ -128,6 +130,31 @@ def paged_chunks(B=4, H=8, H_kv=2, d=128, page_size=64, max_pages=16, num_pages=
     return dict(q=q.to(device), cu_seqlens_q=cu.to(torch.int32).to(device), q_lens=q_lens,
                 seq_lens=seq_lens.to(device), block_table=block_table.to(device), k_cache=k_cache,
                 v_cache=v_cache, used_pages=used, max_q_len=int(q_lens.max()) if B else 0)
+
+
+def varlen_qkv(B=8, H=8, H_kv=2, d=128, q_lo=1, q_hi=512, ctx_lo=0, ctx_hi=0, seed=0, device="cpu"):
+    """Packed variable-length batch: per request q_len uniform in [q_lo, q_hi]
+    new tokens and k_len = q_len + a prefix uniform in [ctx_lo, ctx_hi] keys
+    (ctx 0: self-attention of packed sequences).  The CPU generator draws
+    q_lens, then prefixes, then q [total_q, H, d], k, v [total_k, H_kv, d] as
+    float32 N(0,1) rounded to bf16.  Returns dict(q, k, v, cu_seqlens_q,
+    cu_seqlens_k, max_q_len, max_k_len)."""
+    if H_kv < 1 or H % H_kv:
+        raise ValueError("H_kv must divide H")
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    q_lens = torch.randint(q_lo, q_hi + 1, (B,), generator=g, dtype=torch.int64)
+    ctx = torch.randint(ctx_lo, ctx_hi + 1, (B,), generator=g, dtype=torch.int64)
+    k_lens = q_lens + ctx
+    cu_q = torch.zeros(B + 1, dtype=torch.int64)
+    cu_q[1:] = torch.cumsum(q_lens, 0)
+    cu_k = torch.zeros(B + 1, dtype=torch.int64)
+    cu_k[1:] = torch.cumsum(k_lens, 0)
+    q = torch.randn((int(cu_q[-1]), H, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    k = torch.randn((int(cu_k[-1]), H_kv, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    v = torch.randn((int(cu_k[-1]), H_kv, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    return dict(q=q.to(device), k=k.to(device), v=v.to(device), cu_seqlens_q=cu_q.to(torch.int32).to(device),
+                cu_seqlens_k=cu_k.to(torch.int32).to(device), max_q_len=int(q_lens.max()) if B else 0,
+                max_k_len=int(k_lens.max()) if B else 0)
 
 
 def sample_rows(BH, Nq, n_random=4096, tile=128, seed=0):

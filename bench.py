@@ -14,7 +14,9 @@ Also reported in the same JSON line (timed the same way, not part of
 pages), the same decode with 32 query heads over 8 KV heads on the tensor
 cores -- both as HBM GB/s of algorithmic bytes -- and causal prefill chunks
 over a paged cache (8 requests x 2048 new tokens after 6144 cached, 32 query
-heads over 8 KV heads) as TFLOPS of exactly counted visible pairs.
+heads over 8 KV heads) and a variable-length causal batch (16 packed sequences of 512..4096
+tokens, 32 query heads over 8 KV heads) as TFLOPS of exactly counted
+visible pairs.
 
 `--impl reference` times the float64 CPU oracle (the only reference this
 method has) on a bounded row sample of the same workload.
@@ -455,6 +457,29 @@ def run_secondary(torch, attn, inputs, dev, flush, peaks, rank):
     tf = f / (statistics.mean(ms) * 1e-3) / 1e12
     out["paged_prefill_chunks_8x2048_over_6144_H32_Hkv8_d128_causal"] = {
         "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
+        "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4),
+        "flops_note": "4 * d * H * visible (query, key) pairs, counted exactly"}
+    del p, o, l, ws
+    torch.cuda.empty_cache()
+    # variable-length batch prefill: 16 packed sequences of 512..4096 tokens, causal self-attention
+    p = inputs.varlen_qkv(B=16, H=32, H_kv=8, d=128, q_lo=512, q_hi=4096, seed=rank, device=dev)
+    o = torch.empty_like(p["q"])
+    l = torch.empty((p["q"].shape[0], 32), dtype=torch.float32, device=dev)
+    ws = torch.empty(attn.attn_varlen_fwd_workspace_size(16, p["q"].shape[0], p["max_q_len"], p["max_k_len"], 32, 8,
+                                                         128), dtype=torch.uint8, device=dev)
+
+    def varlen():
+        attn.varlen_fwd(p["q"], p["k"], p["v"], p["cu_seqlens_q"], p["cu_seqlens_k"], max_q_len=p["max_q_len"],
+                        max_k_len=p["max_k_len"], causal=True, out=o, lse=l, workspace=ws)
+    varlen()
+    ms = timed_launches(torch, varlen, reps, flush)
+    attn.device_status()
+    lens = (p["cu_seqlens_q"][1:] - p["cu_seqlens_q"][:-1]).long().cpu()
+    pairs = int((lens * (lens + 1) // 2).sum())  # query i of a sequence sees i + 1 keys
+    f = 4.0 * pairs * 32 * 128
+    tf = f / (statistics.mean(ms) * 1e-3) / 1e12
+    out["varlen_prefill_16seq_512-4096_H32_Hkv8_d128_causal"] = {
+        "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4), "tokens": int(lens.sum()),
         "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4),
         "flops_note": "4 * d * H * visible (query, key) pairs, counted exactly"}
     del p, o, l, ws

@@ -190,6 +190,35 @@ attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_c
                              int max_pages_per_seq, int num_pages, float scale, int causal,
                              void* o, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace attn_varlen_fwd needs (0 on invalid sizes); the
+ * same layout as for attn_paged_fwd. */
+size_t attn_varlen_fwd_workspace_size(int B, int total_q, int max_q_len, int max_k_len, int H, int H_kv, int d);
+
+/* Variable-length batch prefill: B independent attention problems packed
+ * back to back without padding, grouped KV heads as in attn_paged_fwd (the
+ * same kernel, reading K/V rows directly instead of through a page table).
+ *   q: bf16 [total_q, H, d]; request r owns query rows
+ *     cu_seqlens_q[r] .. cu_seqlens_q[r+1]-1
+ *   k, v: bf16 [total_k, H_kv, d]; request r owns key rows
+ *     cu_seqlens_k[r] .. cu_seqlens_k[r+1]-1
+ *   cu_seqlens_q, cu_seqlens_k: int32 [B + 1] device offsets, non-decreasing,
+ *     first 0 and last total_q / total_k; per request at most max_q_len
+ *     queries and max_k_len keys
+ *   causal: 1 = query i of a request with q_len queries and k_len keys sees
+ *     keys t <= i + (k_len - q_len) (the bottom-right aligned lower triangle
+ *     of attn_fwd); 0 = every query sees all of its request's keys
+ *   o: bf16 [total_q, H, d]; lse: fp32 [total_q, H] or NULL
+ *   workspace: at least attn_varlen_fwd_workspace_size(...) bytes,
+ *     caller-owned, 16-byte aligned, no initialisation needed
+ *   d in {64, 128}; H % H_kv == 0 and H / H_kv <= 128.
+ * A query with no visible key gets O = 0 and lse = -inf.  Offsets out of
+ * range set the device status word to ATTN_ERR_DEVICE_DATA (the call's
+ * results are then undefined).  Errors as attn_paged_fwd. */
+attn_status_t attn_varlen_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_k, int B, int total_q, int total_k, int max_q_len,
+                              int max_k_len, int H, int H_kv, int d, float scale, int causal, void* o,
+                              float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then reads and clears the calling device's status
  * word.  Kernels set it when a bounded internal wait gives up
  * (ATTN_ERR_TIMEOUT; the kernel then returns early and its outputs are

@@ -15,6 +15,8 @@ Parity status of each function (the pins live in tests/test_oracle_pins.py):
                  whose KV heads are repeated; prefill chunks equal dense
                  bottom-right causal attention on the gathered keys; one
                  token per request equals paged_decode; closed forms)
+  varlen_attention pinned (equal to dense bottom-right causal attention per
+                 request; it is paged_attention on one-row pages)
   decode_elems   pinned (bf16 / e4m3fn codes against torch's conversions)
 """
 from .oracle import (  # noqa: F401
@@ -25,4 +27,5 @@ from .oracle import (  # noqa: F401
     default_threads,
     paged_attention,
     paged_decode,
+    varlen_attention,
 )

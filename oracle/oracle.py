@@ -210,6 +210,30 @@ def paged_attention(q, k_cache, v_cache, block_table, seq_lens, scale, cu_seqlen
     return res + (psum.reshape(total_q, H),) if with_psum else res
 
 
+def varlen_attention(q, k, v, cu_seqlens_q, cu_seqlens_k, scale, causal=False, nthreads=None):
+    """Variable-length batch attention: request r owns query rows
+    cu_seqlens_q[r] .. cu_seqlens_q[r+1]-1 of q [total_q, H, d] and key rows
+    cu_seqlens_k[r] .. cu_seqlens_k[r+1]-1 of k, v [total_k, H_kv, d].
+
+    The same computation as paged_attention on a cache of one-row pages
+    (k viewed as [total_k, 1, H_kv, d]) whose table lists request r's rows in
+    order; causal: query i sees keys t <= i + (k_len - q_len).  Returns
+    (o [total_q, H, d], lse [total_q, H]).
+    """
+    import torch
+    cu_q = torch.as_tensor(_to_numpy(cu_seqlens_q), dtype=torch.int32)
+    cu_k = torch.as_tensor(_to_numpy(cu_seqlens_k), dtype=torch.int32)
+    B = cu_k.shape[0] - 1
+    lens = (cu_k[1:] - cu_k[:-1]).to(torch.int32)
+    width = max(1, int(lens.max())) if B else 1
+    table = torch.full((B, width), -1, dtype=torch.int32)
+    for r in range(B):
+        n = int(lens[r])
+        table[r, :n] = torch.arange(int(cu_k[r]), int(cu_k[r]) + n, dtype=torch.int32)
+    return paged_attention(q, k.unsqueeze(1), v.unsqueeze(1), table, lens, scale, cu_seqlens_q=cu_q,
+                           causal=causal, nthreads=nthreads)
+
+
 def decode_elems(x):
     """Widen every element of x (bf16 / e4m3fn / f32 / f64) to float64 via the C decoder."""
     lib = build()

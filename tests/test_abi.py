@@ -28,6 +28,7 @@ def test_header_declares_the_entry_points():
     assert _declared() == sorted(["attn_fwd", "attn_fwd_fp8", "attn_paged_decode",
                                   "attn_paged_decode_workspace_size", "attn_paged_decode_noalloc",
                                   "attn_paged_fwd", "attn_paged_fwd_workspace_size",
+                                  "attn_varlen_fwd", "attn_varlen_fwd_workspace_size",
                                   "attn_device_status", "attn_status_string"])
 
 
@@ -148,3 +149,18 @@ def test_paged_fwd_validation(L):
     assert ws > 0
     assert attn.attn_paged_fwd(**long) == attn.ATTN_ERR_WORKSPACE
     assert attn.attn_paged_fwd(**dict(long, workspace=FAKE, workspace_bytes=ws - 1)) == attn.ATTN_ERR_WORKSPACE
+
+
+def test_varlen_fwd_validation(L):
+    ws = attn.attn_varlen_fwd_workspace_size(4, 64, 32, 48, 8, 2, 128)
+    assert ws > 0
+    assert attn.attn_varlen_fwd_workspace_size(4, 64, 32, 0, 8, 2, 128) == 0
+    assert attn.attn_varlen_fwd_workspace_size(4, 64, 32, 48, 8, 3, 128) == 0
+    base = dict(q=FAKE, k=FAKE, v=FAKE, cu_seqlens_q=FAKE, cu_seqlens_k=FAKE, B=4, total_q=64, total_k=100,
+                max_q_len=32, max_k_len=48, H=8, H_kv=2, d=128, scale=0.088, causal=1, o=FAKE, lse=None,
+                workspace=FAKE, workspace_bytes=ws, stream=None)
+    assert attn.attn_varlen_fwd(**dict(base, cu_seqlens_k=None)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_varlen_fwd(**dict(base, max_k_len=101)) == attn.ATTN_ERR_INVALID_ARG  # > total_k
+    assert attn.attn_varlen_fwd(**dict(base, d=80)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_varlen_fwd(**dict(base, workspace_bytes=ws - 1)) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_varlen_fwd(**dict(base, cu_seqlens_q=FAKE + 2)) == attn.ATTN_ERR_INVALID_ARG

@@ -1,0 +1,71 @@
+"""Variable-length batch prefill (attn_varlen_fwd) parity against the float64 oracle.
+
+Packed self-attention batches (causal and not), prefixes longer than the new
+tokens, grouped KV heads from G = 1 to 8, d = 64 and 128, empty requests,
+requests with more queries than keys, one-token queries over long keys, and
+key ranges split over several CTAs and merged.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_attn_fwd_03_gb300 as attn
+import oracle
+from attention_attn_fwd_03_gb300 import inputs
+
+from _parity import TOL_LSE, TOL_O_BF16, compare, default_scale
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    attn.lib()
+
+
+def _run(p, scale, causal):
+    d = {k: (v.to(DEV) if isinstance(v, torch.Tensor) else v) for k, v in p.items()}
+    o, lse = attn.varlen_fwd(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"], max_q_len=d["max_q_len"],
+                             max_k_len=d["max_k_len"], causal=causal, scale=scale)
+    attn.device_status()
+    return o, lse
+
+
+def _ref(p, scale, causal):
+    return oracle.varlen_attention(p["q"], p["k"], p["v"], p["cu_seqlens_q"], p["cu_seqlens_k"], scale, causal=causal)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,H,H_kv,d,q_lo,q_hi,ctx_lo,ctx_hi", [
+    (6, 8, 2, 128, 1, 700, 0, 0),          # packed self-attention
+    (4, 4, 4, 64, 0, 300, 0, 200),         # G = 1, d = 64, empty requests possible
+    (3, 16, 2, 128, 1000, 1500, 0, 3000),  # G = 8, few units: key ranges split and merged
+    (8, 32, 8, 128, 1, 1, 100, 3000),      # one query per request over long keys
+])
+def test_varlen(B, H, H_kv, d, q_lo, q_hi, ctx_lo, ctx_hi, causal):
+    p = inputs.varlen_qkv(B=B, H=H, H_kv=H_kv, d=d, q_lo=q_lo, q_hi=q_hi, ctx_lo=ctx_lo, ctx_hi=ctx_hi,
+                          seed=B * 31 + H + d)
+    scale = default_scale(d)
+    o, lse = _run(p, scale, causal)
+    o_ref, l_ref = _ref(p, scale, causal)
+    compare("varlen_%dx%d/%d_d%d_q%d-%d_ctx%d-%d_%s" % (B, H, H_kv, d, q_lo, q_hi, ctx_lo, ctx_hi,
+                                                        "causal" if causal else "full"),
+            o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+def test_varlen_more_queries_than_keys():
+    """Under the causal mask the first q_len - k_len queries see no key."""
+    p = inputs.varlen_qkv(B=3, H=8, H_kv=4, d=128, q_lo=200, q_hi=300, seed=41)
+    cu_q, cu_k = p["cu_seqlens_q"], p["cu_seqlens_k"].clone()
+    lens = cu_k[1:] - cu_k[:-1]
+    new_lens = torch.tensor([int(lens[0]) // 3, int(lens[1]), 0], dtype=torch.int64)
+    keep = torch.cat([torch.arange(int(cu_k[r]), int(cu_k[r]) + int(new_lens[r])) for r in range(3)])
+    p["k"], p["v"] = p["k"][keep].contiguous(), p["v"][keep].contiguous()
+    p["cu_seqlens_k"] = torch.cat([torch.zeros(1, dtype=torch.int64), torch.cumsum(new_lens, 0)]).to(torch.int32)
+    p["max_k_len"] = int(new_lens.max())
+    scale = default_scale(128)
+    o, lse = _run(p, scale, True)
+    o_ref, l_ref = _ref(p, scale, True)
+    assert np.isneginf(l_ref).any()
+    compare("varlen_short_keys", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)

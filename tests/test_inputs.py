@@ -86,3 +86,13 @@ def test_grouped_cache_keeps_the_draw_order():
                         H_kv=2)
     assert torch.equal(a["q"], b["q"]) and torch.equal(a["block_table"], b["block_table"])
     assert b["k_cache"].shape == (16, 4, 2, 8)
+
+
+def test_varlen_inputs_structure():
+    p = inputs.varlen_qkv(B=6, H=4, H_kv=2, d=8, q_lo=0, q_hi=7, ctx_lo=1, ctx_hi=5, seed=6)
+    cu_q, cu_k = p["cu_seqlens_q"], p["cu_seqlens_k"]
+    assert cu_q.shape == (7,) and cu_k.shape == (7,) and int(cu_q[0]) == 0 and int(cu_k[0]) == 0
+    ql, kl = cu_q[1:] - cu_q[:-1], cu_k[1:] - cu_k[:-1]
+    assert bool((kl - ql >= 1).all()) and bool((kl - ql <= 5).all())
+    assert p["q"].shape == (int(cu_q[-1]), 4, 8) and p["k"].shape == (int(cu_k[-1]), 2, 8)
+    assert p["max_q_len"] == int(ql.max()) and p["max_k_len"] == int(kl.max())

@@ -489,3 +489,38 @@ def test_paged_attention_rejects_bad_offsets():
     with pytest.raises(oracle.OracleError):
         oracle.paged_attention(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], 1.0,
                                cu_seqlens_q=torch.tensor([0, 2, 1], dtype=torch.int32))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_equals_dense_attention_per_request(causal):
+    """A packed variable-length batch is B independent dense problems; with
+    the causal mask each one is aligned bottom-right (k_len >= q_len here,
+    and one request with more queries than keys exercises rows that see no
+    key)."""
+    p = inputs.varlen_qkv(B=5, H=4, H_kv=2, d=8, q_lo=0, q_hi=9, ctx_lo=0, ctx_hi=6, seed=16)
+    cu_q, cu_k = p["cu_seqlens_q"].clone(), p["cu_seqlens_k"].clone()
+    q, k, v = p["q"], p["k"], p["v"]
+    # shrink request 2's keys below its queries (rows with no key under the causal mask)
+    r = 2
+    qn, kn = int(cu_q[r + 1] - cu_q[r]), int(cu_k[r + 1] - cu_k[r])
+    drop = max(0, kn - max(0, qn - 3))
+    if drop:
+        a = int(cu_k[r + 1]) - drop
+        k = torch.cat([k[:a], k[a + drop:]]); v = torch.cat([v[:a], v[a + drop:]])
+        cu_k[r + 1:] -= drop
+    o, lse = oracle.varlen_attention(q, k, v, cu_q, cu_k, 0.3, causal=causal)
+    for rr in range(5):
+        a, b = int(cu_q[rr]), int(cu_q[rr + 1])
+        ka, kb = int(cu_k[rr]), int(cu_k[rr + 1])
+        if a == b:
+            continue
+        qd = q[a:b].transpose(0, 1).contiguous()
+        kd = k[ka:kb].transpose(0, 1).repeat_interleave(2, dim=0).contiguous()
+        vd = v[ka:kb].transpose(0, 1).repeat_interleave(2, dim=0).contiguous()
+        if kb == ka:
+            assert np.all(o[a:b] == 0) and np.all(np.isneginf(lse[a:b]))
+            continue
+        od, ld = oracle.attention(qd, kd, vd, scale=0.3, causal=causal)
+        assert np.array_equal(o[a:b], od.transpose(1, 0, 2)) and np.array_equal(lse[a:b], ld.T)
+    if causal:
+        assert np.isneginf(lse).any()
