@@ -10,6 +10,8 @@ numpy / torch CPU arrays into it.
 
 Parity status of each function (the pins live in tests/test_oracle_pins.py):
   attention      pinned (worked example, closed forms, tiled-vs-naive, mpmath)
+  attention_bwd  pinned (central finite differences of attention, softmax
+                 shift invariance, constant-value and probability-sum identities)
   paged_decode   pinned (equal to attention on the gathered keys; table invariance)
   paged_attention pinned (grouped heads equal multi-head attention on a cache
                  whose KV heads are repeated; prefill chunks equal dense
@@ -22,6 +24,7 @@ Parity status of each function (the pins live in tests/test_oracle_pins.py):
 from .oracle import (  # noqa: F401
     OracleError,
     attention,
+    attention_bwd,
     build,
     decode_elems,
     default_threads,

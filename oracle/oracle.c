@@ -49,6 +49,20 @@
  *     causal mask, sees keys t <= that position (the bottom-right alignment
  *     used for dense attention).
  *
+ * Backward (oracle_attention_bwd): the gradients of the same definition.
+ * The pages keep only the row statistics of the forward pass and recompute
+ * P from Q and K when gradients are needed ("Capstone", section 6.1, the
+ * pitfalls table, and section 7.3, question 1); the gradient formulas are the
+ * chain rule applied to the definition, written out for one row i with
+ * upstream gradient dO_i:
+ *   o_i   = sum_j p_ij v_j,   p_ij = exp(s_ij - lse_i),  s_ij = scale q_i.k_j
+ *   dV_j += p_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   D_i   = dO_i . o_i        (= sum_j p_ij dP_ij)
+ *   dS_ij = p_ij (dP_ij - D_i)   (the softmax Jacobian applied to dP)
+ *   dQ_i  = scale sum_j dS_ij k_j,   dK_j += scale dS_ij q_i
+ * Masked (invisible) keys have p_ij = 0 and contribute nothing.
+ *
  * Input element types: float64, float32, bfloat16 bit patterns, e4m3fn bit
  * patterns.  bf16 and e4m3fn are decoded from their bit-level definitions.
  */
@@ -380,4 +394,121 @@ int oracle_paged_attention(const void* q, int q_dt,
     jb.n_rows = total_q * H;
     jb.o = o; jb.lse = lse; jb.psum = psum;
     return run_job(&jb, nthreads);
+}
+
+/* ---- backward ---------------------------------------------------------- */
+
+typedef struct {
+    const void* q; const void* k; const void* v; const void* dout; int dt;
+    int64_t BH, Nq, Nk; int d; double scale; int causal;
+    double* dq; double* dk; double* dv;
+    int64_t next;
+    int err;
+} bwd_job_t;
+
+/* One (batch, head) per work item: its dK and dV accumulate over all rows. */
+static void* bwd_worker(void* arg) {
+    bwd_job_t* jb = (bwd_job_t*)arg;
+    const int d = jb->d;
+    const int64_t Nq = jb->Nq, Nk = jb->Nk;
+    double* kk = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1) * d);
+    double* vv = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1) * d);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+    double* dp = (double*)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+    double* qr = (double*)malloc(sizeof(double) * d);
+    double* gr = (double*)malloc(sizeof(double) * d);
+    double* o = (double*)malloc(sizeof(double) * d);
+    if (!kk || !vv || !s || !dp || !qr || !gr || !o) {
+        __atomic_store_n(&jb->err, OR_NO_MEM, __ATOMIC_RELAXED);
+        free(kk); free(vv); free(s); free(dp); free(qr); free(gr); free(o);
+        return NULL;
+    }
+    for (;;) {
+        int64_t bh = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (bh >= jb->BH) break;
+        int64_t i, j;
+        int c;
+        load_row(jb->k, jb->dt, bh * Nk * d, (int)(Nk * d), 1.0, kk);
+        load_row(jb->v, jb->dt, bh * Nk * d, (int)(Nk * d), 1.0, vv);
+        double* dK = jb->dk + bh * Nk * d;
+        double* dV = jb->dv + bh * Nk * d;
+        for (j = 0; j < Nk * d; ++j) { dK[j] = 0.0; dV[j] = 0.0; }
+        for (i = 0; i < Nq; ++i) {
+            double* dQ = jb->dq + (bh * Nq + i) * d;
+            for (c = 0; c < d; ++c) dQ[c] = 0.0;
+            int64_t n = Nk;
+            if (jb->causal) {
+                n = i + (Nk - Nq) + 1; /* bottom-right aligned */
+                if (n < 0) n = 0;
+                if (n > Nk) n = Nk;
+            }
+            if (n == 0) continue;
+            load_row(jb->q, jb->dt, (bh * Nq + i) * d, d, 1.0, qr);
+            load_row(jb->dout, jb->dt, (bh * Nq + i) * d, d, 1.0, gr);
+            /* forward for the row: scores, max, denominator, probabilities, o */
+            double m = -INFINITY;
+            for (j = 0; j < n; ++j) {
+                double acc = 0.0;
+                for (c = 0; c < d; ++c) acc += qr[c] * kk[j * d + c];
+                s[j] = jb->scale * acc;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (j = 0; j < n; ++j) l += exp(s[j] - m);
+            for (c = 0; c < d; ++c) o[c] = 0.0;
+            for (j = 0; j < n; ++j) {
+                s[j] = exp(s[j] - m) / l; /* s now holds p_ij */
+                for (c = 0; c < d; ++c) o[c] += s[j] * vv[j * d + c];
+            }
+            /* D_i = dO_i . o_i, dP_ij = dO_i . v_j */
+            double D = 0.0;
+            for (c = 0; c < d; ++c) D += gr[c] * o[c];
+            for (j = 0; j < n; ++j) {
+                double acc = 0.0;
+                for (c = 0; c < d; ++c) acc += gr[c] * vv[j * d + c];
+                dp[j] = acc;
+            }
+            for (j = 0; j < n; ++j) {
+                const double p = s[j];
+                const double ds = p * (dp[j] - D);
+                for (c = 0; c < d; ++c) {
+                    dV[j * d + c] += p * gr[c];
+                    dQ[c] += jb->scale * ds * kk[j * d + c];
+                    dK[j * d + c] += jb->scale * ds * qr[c];
+                }
+            }
+        }
+    }
+    free(kk); free(vv); free(s); free(dp); free(qr); free(gr); free(o);
+    return NULL;
+}
+
+/* Gradients of dense attention with respect to q, k, v for the upstream
+ * gradient dout.  q, dout: [BH, Nq, d]; k, v: [BH, Nk, d]; all of element
+ * type dt.  dq: [BH, Nq, d], dk, dv: [BH, Nk, d] float64.  Rows with no
+ * visible key have zero gradients. */
+int oracle_attention_bwd(const void* q, const void* k, const void* v, const void* dout, int dt,
+                         int64_t BH, int64_t Nq, int64_t Nk, int d, double scale, int causal,
+                         double* dq, double* dk, double* dv, int nthreads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || !dtype_ok(dt)) return OR_BAD_ARG;
+    if (BH < 0 || Nq < 0 || Nk < 0 || d < 1 || d > 4096 || Nk * d > 0x7fffffffLL) return OR_BAD_ARG;
+    bwd_job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.q = q; jb.k = k; jb.v = v; jb.dout = dout; jb.dt = dt;
+    jb.BH = BH; jb.Nq = Nq; jb.Nk = Nk; jb.d = d; jb.scale = scale; jb.causal = causal;
+    jb.dq = dq; jb.dk = dk; jb.dv = dv;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    if ((int64_t)nthreads > BH) nthreads = BH > 0 ? (int)BH : 1;
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * nthreads);
+    if (!th) return OR_NO_MEM;
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, bwd_worker, &jb) != 0) break;
+        ++started;
+    }
+    if (started == 0) bwd_worker(&jb);
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    free(th);
+    return jb.err;
 }

@@ -48,6 +48,8 @@ def build(force=False):
             lib.oracle_paged_attention.restype = i
             lib.oracle_paged_attention.argtypes = [vp, i, vp, vp, i, vp, vp, vp, i, i64, i, i, i, i, i, i64,
                                                    dbl, i, vp, vp, vp, i]
+            lib.oracle_attention_bwd.restype = i
+            lib.oracle_attention_bwd.argtypes = [vp, vp, vp, vp, i, i64, i64, i64, i, dbl, i, vp, vp, vp, i]
             lib.oracle_decode.restype = i
             lib.oracle_decode.argtypes = [vp, i, i64, vp]
             _lib = lib
@@ -164,6 +166,32 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale, nthreads=Non
     _check(rc)
     res = (o.reshape(B, H, d), lse.reshape(B, H))
     return res + (psum.reshape(B, H),) if with_psum else res
+
+
+def attention_bwd(q, k, v, dout, scale, causal=False, nthreads=None):
+    """Gradients (dq, dk, dv) of attention(q, k, v) for the upstream gradient
+    dout, all BHSD: q, dout [.., Nq, d], k, v [.., Nk, d] of one element type.
+    Returned as float64 arrays shaped like q, k, v."""
+    lib = build()
+    qa, qd = _as_raw(q)
+    ka, kd = _as_raw(k)
+    va, vd = _as_raw(v)
+    ga, gd = _as_raw(dout)
+    if len({qd, kd, vd, gd}) != 1:
+        raise OracleError("q, k, v and dout must share one element type")
+    if ga.shape != qa.shape or va.shape != ka.shape or ka.shape[:-2] != qa.shape[:-2] or ka.shape[-1] != qa.shape[-1]:
+        raise OracleError("shape mismatch")
+    lead = qa.shape[:-2]
+    Nq, d = qa.shape[-2], qa.shape[-1]
+    Nk = ka.shape[-2]
+    BH = int(np.prod(lead)) if lead else 1
+    dq = np.empty(qa.shape, dtype=np.float64)
+    dk = np.empty(ka.shape, dtype=np.float64)
+    dv = np.empty(ka.shape, dtype=np.float64)
+    _check(lib.oracle_attention_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(ga), qd, BH, Nq, Nk, d, float(scale),
+                                    int(bool(causal)), _ptr(dq), _ptr(dk), _ptr(dv),
+                                    int(nthreads or default_threads())))
+    return dq, dk, dv
 
 
 def paged_attention(q, k_cache, v_cache, block_table, seq_lens, scale, cu_seqlens_q=None, causal=False,

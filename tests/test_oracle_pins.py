@@ -524,3 +524,81 @@ def test_varlen_equals_dense_attention_per_request(causal):
         assert np.array_equal(o[a:b], od.transpose(1, 0, 2)) and np.array_equal(lse[a:b], ld.T)
     if causal:
         assert np.isneginf(lse).any()
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(q, k, v, dout, scale, causal):
+    o, _ = oracle.attention(q, k, v, scale=scale, causal=causal)
+    return float(np.sum(o * dout))
+
+
+@pytest.mark.parametrize("Nq,Nk,causal", [(3, 5, False), (4, 4, True), (5, 3, True), (2, 6, True)])
+def test_backward_equals_finite_differences(Nq, Nk, causal):
+    """The gradient of L = sum(dO * O) by central differences of the forward
+    oracle (step 1e-5, truncation error ~1e-10) agrees with the backward
+    oracle for every element of q, k and v; with Nq > Nk under the causal mask
+    some rows see no key and must get zero gradients."""
+    rng = np.random.default_rng(Nq * 10 + Nk)
+    BH, d, scale = 2, 3, 0.7
+    q = rng.standard_normal((BH, Nq, d))
+    k = rng.standard_normal((BH, Nk, d))
+    v = rng.standard_normal((BH, Nk, d))
+    dout = rng.standard_normal((BH, Nq, d))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dout, scale, causal=causal)
+    h = 1e-5
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = {"q": q, "k": k, "v": v}
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (_loss(args_p["q"], args_p["k"], args_p["v"], dout, scale, causal) -
+                        _loss(args_m["q"], args_m["k"], args_m["v"], dout, scale, causal)) / (2 * h)
+        assert np.allclose(g, num, rtol=0, atol=2e-8), name
+
+
+def test_backward_identities():
+    """Softmax is invariant to a common shift of a row's scores, so every
+    row's dS sums to 0 and the dK rows of a head sum to 0; probabilities sum
+    to 1, so the dV rows sum to the dO rows; constant value rows make O
+    independent of q and k, so dQ = dK = 0."""
+    rng = np.random.default_rng(5)
+    BH, Nq, Nk, d = 3, 7, 9, 4
+    q = rng.standard_normal((BH, Nq, d))
+    k = rng.standard_normal((BH, Nk, d))
+    v = rng.standard_normal((BH, Nk, d))
+    dout = rng.standard_normal((BH, Nq, d))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dout, 0.5)
+    assert np.allclose(dk.sum(axis=1), 0.0, atol=1e-12)
+    assert np.allclose(dv.sum(axis=1), dout.sum(axis=1), atol=1e-12)
+    vc = np.broadcast_to(rng.standard_normal((BH, 1, d)), (BH, Nk, d)).copy()
+    dq0, dk0, _ = oracle.attention_bwd(q, k, vc, dout, 0.5)
+    assert np.allclose(dq0, 0.0, atol=1e-12) and np.allclose(dk0, 0.0, atol=1e-12)
+
+
+def test_backward_causal_first_row():
+    """Under the causal mask query 0 sees only key 0 (p = 1): its dQ is 0 and
+    key 0's dV receives all of dO_0."""
+    rng = np.random.default_rng(6)
+    q, k, v, dout = (rng.standard_normal((1, 4, 3)) for _ in range(4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dout, 1.0, causal=True)
+    assert np.allclose(dq[0, 0], 0.0, atol=1e-14)
+    # key 3 is seen only by query 3, key 0 by all four queries
+    o, _ = oracle.attention(q, k, v, scale=1.0, causal=True)
+    assert np.all(np.isfinite(dv)) and np.allclose(dv.sum(axis=1), dout.sum(axis=1), atol=1e-12)
+
+
+def test_backward_bf16_inputs_are_decoded_exactly():
+    """bf16 inputs give the same gradients as their exact float64 values."""
+    q, k, v = inputs.dense_qkv(1, 2, 6, 8, 16, seed=7)
+    g = torch.Generator().manual_seed(8)
+    dout = torch.randn((1, 2, 6, 16), generator=g).to(torch.bfloat16)
+    a = oracle.attention_bwd(q, k, v, dout, 0.25, causal=True)
+    b = oracle.attention_bwd(q.double().numpy(), k.double().numpy(), v.double().numpy(), dout.double().numpy(),
+                             0.25, causal=True)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
