@@ -8,11 +8,12 @@ Two levels:
   * ``attn_fwd``, ``attn_fwd_fp8``, ``attn_paged_decode``,
     ``attn_paged_decode_workspace_size``, ``attn_paged_decode_noalloc``,
     ``attn_paged_fwd``, ``attn_paged_fwd_workspace_size``,
-    ``attn_varlen_fwd``, ``attn_varlen_fwd_workspace_size``,
+    ``attn_varlen_fwd``, ``attn_varlen_fwd_workspace_size``, ``attn_bwd``,
+    ``attn_bwd_workspace_size``,
     ``attn_device_status``, ``attn_status_string``: the C entry points, same
     names and argument order, taking raw device pointers (ints) and a stream
     handle (int).
-  * ``fwd``, ``fwd_fp8``, ``paged_decode``, ``paged_fwd``, ``varlen_fwd``: take torch CUDA
+  * ``fwd``, ``fwd_fp8``, ``paged_decode``, ``paged_fwd``, ``varlen_fwd``, ``bwd``: take torch CUDA
     tensors, allocate
     outputs with torch when none are given, call the C entry point on the
     current stream and raise ``AttnError`` on a non-zero status.
@@ -84,6 +85,10 @@ def lib():
             L.attn_varlen_fwd_workspace_size.argtypes = [i, i, i, i, i, i, i]
             L.attn_varlen_fwd.restype = i
             L.attn_varlen_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp, sz, vp]
+            L.attn_bwd_workspace_size.restype = sz
+            L.attn_bwd_workspace_size.argtypes = [i, i, i, i]
+            L.attn_bwd.restype = i
+            L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
             L.attn_device_status.restype = i
             L.attn_device_status.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -142,6 +147,16 @@ def attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, B, total_q, total_k, ma
                     scale, causal, o, lse, workspace, workspace_bytes, stream):
     return lib().attn_varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, B, total_q, total_k, max_q_len, max_k_len, H,
                                  H_kv, d, scale, causal, o, lse, workspace, workspace_bytes, stream)
+
+
+def attn_bwd_workspace_size(B, H, Nq, d):
+    return lib().attn_bwd_workspace_size(B, H, Nq, d)
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace, workspace_bytes,
+             stream):
+    return lib().attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace,
+                          workspace_bytes, stream)
 
 
 def attn_device_status(stream):
@@ -355,6 +370,39 @@ def varlen_fwd(q, k, v, cu_seqlens_q, cu_seqlens_k, max_q_len=None, max_k_len=No
                          _stream(stream))
     _raise(st, "attn_varlen_fwd")
     return out, lse
+
+
+def bwd(q, k, v, o, lse, dout, causal=False, scale=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Gradients of fwd: (dq, dk, dv) bf16 for the upstream gradient dout, from
+    the forward inputs q, k, v, its output o and its lse (same scale and
+    causal flag)."""
+    torch = _torch()
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _check(q, "q", torch.bfloat16)
+    _check(k, "k", torch.bfloat16, (B, H, Nk, d))
+    _check(v, "v", torch.bfloat16, (B, H, Nk, d))
+    _check(o, "o", torch.bfloat16, (B, H, Nq, d))
+    _check(dout, "dout", torch.bfloat16, (B, H, Nq, d))
+    _check(lse, "lse", torch.float32, (B, H, Nq))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(dq, "dq", torch.bfloat16, q.shape)
+    _check(dk, "dk", torch.bfloat16, k.shape)
+    _check(dv, "dv", torch.bfloat16, v.shape)
+    ws_bytes = attn_bwd_workspace_size(B, H, Nq, d)
+    if ws_bytes == 0:
+        raise AttnError(ATTN_ERR_UNSUPPORTED, "attn_bwd_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8)
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    st = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                  dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, sc, int(bool(causal)),
+                  workspace.data_ptr(), workspace.numel(), _stream(stream))
+    _raise(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def device_status(stream=None):

@@ -381,6 +381,61 @@ attn_status_t attn_varlen_fwd(const void* q, const void* k, const void* v, const
     return from_cuda(launch_paged(d, p, grid, static_cast<cudaStream_t>(stream)));
 }
 
+size_t attn_bwd_workspace_size(int B, int H, int Nq, int d) {
+    if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128) || (long long)B * H > 65535) return 0;
+    return bwd_workspace_bytes(B * H, Nq, d);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                       float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return ATTN_ERR_INVALID_ARG;
+    if ((long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y holds batch * heads
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv))
+        return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    const int BH = B * H;
+    const size_t need = bwd_workspace_bytes(BH, Nq, d);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+
+    BwdParams p;
+    std::memset(&p, 0, sizeof p);
+    if (!make_map(&p.tm_q, q, false, d, Nq, BH, false) || !make_map(&p.tm_k, k, false, d, Nk, BH, false) ||
+        !make_map(&p.tm_v, v, false, d, Nk, BH, false) || !make_map(&p.tm_do, dout, false, d, Nq, BH, false))
+        return ATTN_ERR_CUDA;
+    const int nq_pad = (Nq + 127) / 128 * 128;
+    char* ws = static_cast<char*>(workspace);
+    p.dq_acc = reinterpret_cast<float*>(ws);
+    p.lse2 = reinterpret_cast<float*>(ws + (size_t)BH * nq_pad * d * sizeof(float));
+    p.dvec = p.lse2 + (size_t)BH * nq_pad;
+    p.o = static_cast<const uint16_t*>(o);
+    p.dout = static_cast<const uint16_t*>(dout);
+    p.lse = lse;
+    p.dq = static_cast<uint16_t*>(dq);
+    p.dk = static_cast<uint16_t*>(dk);
+    p.dv = static_cast<uint16_t*>(dv);
+    p.status = ds->status;
+    p.BH = BH;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.causal = causal;
+    p.n_qblocks = nq_pad / 128;
+    p.n_kblocks = (Nk + 127) / 128;
+    p.nq_pad = nq_pad;
+    p.c_scale = scale * 1.4426950408889634f;
+    p.scale = scale;
+    return from_cuda(launch_bwd(d, p, static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t attn_device_status(void* stream) {
     DeviceState* ds = nullptr;
     attn_status_t st = device_state(&ds);

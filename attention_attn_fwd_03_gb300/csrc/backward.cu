@@ -1,0 +1,474 @@
+// backward.cu -- gradients of exact attention (dQ, dK, dV) by recomputation.
+//
+// The forward pass keeps only the row statistics (here the LSE); the
+// backward pass recomputes the probabilities on chip from Q, K and those
+// statistics instead of reading a stored N x N matrix ("Capstone: CUDA
+// Softmax 与 Attention 算子", section 6.1, the pitfalls table, and section 7.3,
+// question 1).  The gradient of O = softmax(scale Q K^T) V for an upstream
+// gradient dO is, per query row i and key j:
+//   P_ij = 2^(scale log2(e) q_i.k_j - lse_i log2(e)),   D_i = dO_i . O_i
+//   dV_j += P_ij dO_i,   dP_ij = dO_i . v_j,   dS_ij = P_ij (dP_ij - D_i)
+//   dQ_i += scale dS_ij k_j,   dK_j += scale dS_ij q_i
+//
+// Three kernels:
+//   bwd_prep    D = rowsum(dO * O) and lse2 = lse log2(e) (+inf for rows
+//               with no visible key, so their P is 0), both padded to whole
+//               128-row blocks; zeroes the fp32 dQ accumulator.
+//   bwd_main    one CTA per (batch*head, 128-key block j), K_j and V_j
+//               resident in shared memory, looping over the query blocks i
+//               that see any of its keys (all blocks, or from the diagonal on
+//               under the causal mask):
+//                 warp 0    TMA: K_j, V_j once; Q_i and dO_i double-buffered
+//                 warp 1    MMA issuer (one thread):
+//                             S^T = K_j Q_i^T, dP^T = V_j dO_i^T  (TMEM, keys on lanes)
+//                             dV += P^T dO_i, dK += dS^T Q_i       (A = P^T / dS^T from TMEM)
+//                             dQ_i = dS K_j                       (A = dS from shared memory)
+//                 warps 2-5 one thread per key: P^T and dS^T from S^T, dP^T, lse2, D
+//                           (masked pairs: 0); P^T, dS^T back to TMEM as bf16 and dS to
+//                           shared memory in the layout the dQ product reads;
+//                           at the end dK (times scale) and dV -> bf16 -> global
+//                 warps 6-9 one thread per query: dQ_i from TMEM added into the fp32
+//                           accumulator with vector reductions (red.global.add.v4.f32)
+//   bwd_dq      dQ = scale * accumulator -> bf16.
+//
+// Tensor memory: columns 0-127 S^T, then P^T over it, then dQ_i; 128-255
+// dP^T, then dS^T over it; 256.. dV (d columns); 256 + d.. dK (d columns).
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tile_mma.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BCfg {
+    static constexpr int NPANEL = D / 64;
+    static constexpr int PANEL_BYTES = 128 * 128;
+    static constexpr int TILE_BYTES = NPANEL * PANEL_BYTES;  // 128 rows x d bf16
+    static constexpr int DS_BYTES = 2 * PANEL_BYTES;         // 128 keys x 128 queries bf16
+    static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D;
+    static constexpr uint32_t TM_COLS = 512;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + TILE_BYTES;
+    static constexpr int OFF_Q = OFF_V + TILE_BYTES;        // [2]
+    static constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;   // [2]
+    static constexpr int OFF_DS = OFF_DO + 2 * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+    static constexpr int N_BARS = 12;
+    static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
+    static constexpr int SMEM_USED = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = (SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024);
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    // dQ = dS K: A = dS (MN-major: queries contiguous), B = K_j (MN-major: dims contiguous)
+    static constexpr uint32_t ID_DQ = idesc_make(128, D, 1u, true, true);
+};
+
+struct BBars {
+    uint64_t* kv_full;
+    uint64_t* qd_full;   // [2]
+    uint64_t* qd_empty;  // [2]
+    uint64_t* s_full;    // S^T and dP^T computed
+    uint64_t* ds_ready;  // 128 arrivals: P^T, dS^T in TMEM, dS in shared memory
+    uint64_t* dq_full;   // dQ_i computed (also: dS in shared memory consumed)
+    uint64_t* dq_empty;  // 128 arrivals: dQ_i read out of TMEM
+    uint64_t* done;      // all products finished (dK, dV final)
+};
+
+// Query blocks a key block j sees: [i0, n_qb).  Under the causal mask query
+// q sees key k iff k <= q + (Nk - Nq), so block i is needed iff its last
+// query reaches the block's first key.
+__device__ __forceinline__ int first_qblock(const BwdParams& p, int j) {
+    if (!p.causal) return 0;
+    const long long need = (long long)j * 128 - (p.Nk - p.Nq) - 127;  // smallest useful last-query index
+    if (need <= 0) return 0;
+    return (int)((need + 127) / 128);
+}
+
+__device__ __forceinline__ void red_add_v4(float* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "f"(__uint_as_float(a)),
+                 "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(void* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- prep / dq kernels
+
+// One warp per padded query row: D and lse2 (padding rows: D = 0, lse2 =
+// +inf), and the row's dQ accumulator zeroed.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
+    constexpr int PER = D / 32;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= (long long)p.BH * p.nq_pad) return;
+    const int bh = (int)(gw / p.nq_pad), i = (int)(gw % p.nq_pad);
+    float dsum = 0.f, l2 = INFINITY;
+    if (i < p.Nq) {
+        const size_t row = ((size_t)bh * p.Nq + i) * D + lane * PER;
+        const uint16_t* o = p.o + row;
+        const uint16_t* g = p.dout + row;
+#pragma unroll
+        for (int c = 0; c < PER; c += 2) {
+            const uint32_t ow = *reinterpret_cast<const uint32_t*>(o + c);
+            const uint32_t gwd = *reinterpret_cast<const uint32_t*>(g + c);
+            dsum = fmaf(bf16lo_to_f32(ow), bf16lo_to_f32(gwd), dsum);
+            dsum = fmaf(bf16hi_to_f32(ow), bf16hi_to_f32(gwd), dsum);
+        }
+#pragma unroll
+        for (int s = 16; s >= 1; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
+        const float lse = p.lse[(size_t)bh * p.Nq + i];
+        l2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+    }
+    if (lane == 0) {
+        p.dvec[gw] = dsum;
+        p.lse2[gw] = l2;
+    }
+    float* acc = p.dq_acc + (size_t)gw * D + lane * PER;
+#pragma unroll
+    for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams p) {
+    constexpr int PER = D / 32;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= (long long)p.BH * p.Nq) return;
+    const int bh = (int)(gw / p.Nq), i = (int)(gw % p.Nq);
+    const float* acc = p.dq_acc + ((size_t)bh * p.nq_pad + i) * D + lane * PER;
+    uint16_t* dst = p.dq + (size_t)gw * D + lane * PER;
+#pragma unroll
+    for (int c = 0; c < PER; c += 2) *reinterpret_cast<uint32_t*>(dst + c) = pack_bf16(acc[c] * p.scale, acc[c + 1] * p.scale);
+}
+
+// ---------------------------------------------------------------- main kernel roles
+
+template <int D>
+__device__ void bwd_producer(const BwdParams& p, uint8_t* smem, const BBars& b, volatile int* abort_flag, int bh,
+                             int j, int i0, int nqb) {
+    using C = BCfg<D>;
+    tma_prefetch_map(&p.tm_q);
+    tma_prefetch_map(&p.tm_k);
+    tma_prefetch_map(&p.tm_v);
+    tma_prefetch_map(&p.tm_do);
+    bar_arrive_expect_tx(b.kv_full, 2 * C::TILE_BYTES);
+#pragma unroll
+    for (int pn = 0; pn < C::NPANEL; ++pn) {
+        tma_load_3d(smem + C::OFF_K + pn * C::PANEL_BYTES, &p.tm_k, b.kv_full, pn * 64, j * 128, bh);
+        tma_load_3d(smem + C::OFF_V + pn * C::PANEL_BYTES, &p.tm_v, b.kv_full, pn * 64, j * 128, bh);
+    }
+    int issued = 0;
+    for (int it = 0; it < nqb; ++it) {
+        const int s = it & 1;
+        if (it >= 2 && !wait_bar(&b.qd_empty[s], (uint32_t)(((it >> 1) - 1) & 1), abort_flag, p.status)) break;
+        const int i = i0 + it;
+        bar_arrive_expect_tx(&b.qd_full[s], 2 * C::TILE_BYTES);
+#pragma unroll
+        for (int pn = 0; pn < C::NPANEL; ++pn) {
+            tma_load_3d(smem + C::OFF_Q + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q, &b.qd_full[s], pn * 64,
+                        i * 128, bh);
+            tma_load_3d(smem + C::OFF_DO + s * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_do, &b.qd_full[s], pn * 64,
+                        i * 128, bh);
+        }
+        ++issued;
+    }
+    // every copy started here lands before the CTA exits
+    drain_wait(b.kv_full, 0, p.status);
+    for (int it = issued - 2 > 0 ? issued - 2 : 0; it < issued; ++it)
+        drain_wait(&b.qd_full[it & 1], (uint32_t)((it >> 1) & 1), p.status);
+}
+
+template <int D>
+__device__ void bwd_mma(const BwdParams& p, uint8_t* smem, const BBars& b, volatile int* abort_flag, uint32_t tmem,
+                        int nqb) {
+    using C = BCfg<D>;
+    const uint32_t sb = smem_u32(smem);
+    // K-major views (S^T = K Q^T, dP^T = V dO^T) and MN-major views (B of dV, dK, dQ)
+    const uint64_t k_kmaj = sdesc_sw128(sb + C::OFF_K, 16, 1024);
+    const uint64_t v_kmaj = sdesc_sw128(sb + C::OFF_V, 16, 1024);
+    const uint64_t k_mn = sdesc_sw128(sb + C::OFF_K, C::PANEL_BYTES, 1024);
+    const uint64_t ds_mn = sdesc_sw128(sb + C::OFF_DS, C::PANEL_BYTES, 1024);
+    if (!wait_bar(b.kv_full, 0, abort_flag, p.status)) return;
+    for (int it = 0; it < nqb; ++it) {
+        const int s = it & 1;
+        const uint32_t q_addr = sb + C::OFF_Q + s * C::TILE_BYTES, do_addr = sb + C::OFF_DO + s * C::TILE_BYTES;
+        if (!wait_bar(&b.qd_full[s], (uint32_t)((it >> 1) & 1), abort_flag, p.status)) return;
+        // the previous dQ_i has left TMEM (its columns are where S^T goes)
+        if (it > 0 && !wait_bar(b.dq_empty, (uint32_t)((it - 1) & 1), abort_flag, p.status)) return;
+        tc_fence_after();
+        issue_s<D, false>(tmem + C::TM_S, k_kmaj, sdesc_sw128(q_addr, 16, 1024));
+        issue_s<D, false>(tmem + C::TM_DP, v_kmaj, sdesc_sw128(do_addr, 16, 1024));
+        tc_commit(b.s_full);
+        if (!wait_bar(b.ds_ready, (uint32_t)(it & 1), abort_flag, p.status)) return;
+        tc_fence_after();
+        issue_pv<D, false>(tmem + C::TM_DV, tmem + C::TM_S, sdesc_sw128(do_addr, C::PANEL_BYTES, 1024), it > 0);
+        issue_pv<D, false>(tmem + C::TM_DK, tmem + C::TM_DP, sdesc_sw128(q_addr, C::PANEL_BYTES, 1024), it > 0);
+        tc_commit(&b.qd_empty[s]);
+        // dQ_i = dS K_j: 8 steps of 16 keys, both operands advance 16 rows (2 KB)
+        mma4_ss<128, 256, 384, 128, 256, 384, false>(tmem + C::TM_S, ds_mn, k_mn, C::ID_DQ, 0u);
+        mma4_ss<128, 256, 384, 128, 256, 384, false>(tmem + C::TM_S, ds_mn + 512, k_mn + 512, C::ID_DQ, 1u);
+        tc_commit(b.dq_full);
+    }
+}
+
+// One thread per key row (TMEM lane): P^T, dS^T for each query block, then
+// the dK, dV epilogue.
+template <int D>
+__device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, volatile int* abort_flag,
+                            uint32_t tmem, int bh, int j, int i0, int nqb, int wq, int lane) {
+    using C = BCfg<D>;
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::TM_S, tP = tmem + lane_off + C::TM_DP;
+    const int key = j * 128 + row;
+    const bool key_ok = key < p.Nk;
+    const int off = p.Nk - p.Nq;
+    const float cs = p.c_scale;
+    const uint32_t ds_row = smem_u32(smem + C::OFF_DS) + (uint32_t)(row * 128);
+    bool ok = true;
+    for (int it = 0; ok && it < nqb; ++it) {
+        const int i = i0 + it;
+        ok = __all_sync(0xffffffffu, wait_bar(b.s_full, (uint32_t)(it & 1), abort_flag, p.status));
+        if (!ok) break;
+        // dS in shared memory is free once the previous block's dQ product read it
+        if (it > 0) {
+            ok = __all_sync(0xffffffffu, wait_bar(b.dq_full, (uint32_t)((it - 1) & 1), abort_flag, p.status));
+            if (!ok) break;
+        }
+        tc_fence_after();
+        // first query of the block that sees this key (earlier queries are masked)
+        const long long q_min = (long long)key - off;
+        const float* l2 = p.lse2 + ((size_t)bh * p.nq_pad + (size_t)i * 128);
+        const float* dv = p.dvec + ((size_t)bh * p.nq_pad + (size_t)i * 128);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {  // 32 queries per chunk
+            uint32_t sv[32], dp[32];
+            tmem_ld32(tS + 32 * c, sv);
+            tmem_ld32(tP + 32 * c, dp);
+            tmem_ld_wait();
+            reg_after_wait<32>(sv);
+            reg_after_wait<32>(dp);
+            uint32_t pw[16], dw[16];
+#pragma unroll
+            for (int t4 = 0; t4 < 8; ++t4) {
+                const float4 L = *reinterpret_cast<const float4*>(l2 + 32 * c + 4 * t4);
+                const float4 Dv = *reinterpret_cast<const float4*>(dv + 32 * c + 4 * t4);
+                const float Ls[4] = {L.x, L.y, L.z, L.w};
+                const float Ds[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+                float pv[4], ds[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int t = 4 * t4 + e;
+                    const long long q = (long long)i * 128 + 32 * c + t;
+                    const bool vis = key_ok && (!p.causal || q >= q_min);
+                    pv[e] = vis ? ex2(fmaf(__uint_as_float(sv[t]), cs, -Ls[e])) : 0.f;
+                    ds[e] = pv[e] * (__uint_as_float(dp[t]) - Ds[e]);
+                }
+                pw[2 * t4] = pack_bf16(pv[0], pv[1]);
+                pw[2 * t4 + 1] = pack_bf16(pv[2], pv[3]);
+                dw[2 * t4] = pack_bf16(ds[0], ds[1]);
+                dw[2 * t4 + 1] = pack_bf16(ds[2], ds[3]);
+            }
+            tmem_st16(tS + 16 * c, pw);
+            tmem_st16(tP + 16 * c, dw);
+            // dS row `row`, queries 32c..32c+31: panel c / 2, 16-byte chunks
+            // (c % 2) * 4 .. +3 of the row, 128-byte swizzle (chunk ^ row % 8)
+            const uint32_t prow = ds_row + (uint32_t)((c >> 1) * C::PANEL_BYTES);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t chunk = (uint32_t)((c & 1) * 4 + k) ^ (uint32_t)(row & 7);
+                st_shared_v4(prow + chunk * 16u, dw[4 * k], dw[4 * k + 1], dw[4 * k + 2], dw[4 * k + 3]);
+            }
+        }
+        tmem_st_wait();
+        fence_async_smem();
+        tc_fence_before();
+        bar_arrive(b.ds_ready);
+    }
+    if (!ok) return;
+    // ---- epilogue: dV and scale * dK rows of this key block -> bf16
+    if (nqb > 0) {
+        ok = __all_sync(0xffffffffu, wait_bar(b.done, 0, abort_flag, p.status));
+        if (!ok) return;
+        tc_fence_after();
+    }
+    uint16_t* dvr = p.dv + ((size_t)bh * p.Nk + key) * D;
+    uint16_t* dkr = p.dk + ((size_t)bh * p.Nk + key) * D;
+#pragma unroll 1
+    for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t a[32], g[32];
+        if (nqb > 0) {
+            tmem_ld32(tmem + lane_off + C::TM_DV + 32 * ch, a);
+            tmem_ld32(tmem + lane_off + C::TM_DK + 32 * ch, g);
+            tmem_ld_wait();
+            reg_after_wait<32>(a);
+            reg_after_wait<32>(g);
+        } else {  // no query sees this block: zero gradients
+#pragma unroll
+            for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
+        }
+        if (key_ok) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+                st_global_v4(dvr + 32 * ch + e, pack_bf16(__uint_as_float(a[e]), __uint_as_float(a[e + 1])),
+                             pack_bf16(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3])),
+                             pack_bf16(__uint_as_float(a[e + 4]), __uint_as_float(a[e + 5])),
+                             pack_bf16(__uint_as_float(a[e + 6]), __uint_as_float(a[e + 7])));
+                const float sc = p.scale;
+                st_global_v4(dkr + 32 * ch + e,
+                             pack_bf16(__uint_as_float(g[e]) * sc, __uint_as_float(g[e + 1]) * sc),
+                             pack_bf16(__uint_as_float(g[e + 2]) * sc, __uint_as_float(g[e + 3]) * sc),
+                             pack_bf16(__uint_as_float(g[e + 4]) * sc, __uint_as_float(g[e + 5]) * sc),
+                             pack_bf16(__uint_as_float(g[e + 6]) * sc, __uint_as_float(g[e + 7]) * sc));
+            }
+        }
+    }
+}
+
+// One thread per query row of the block (TMEM lane): dQ_i added into the
+// accumulator (padded rows, so every row of a block exists).
+template <int D>
+__device__ void bwd_dq_role(const BwdParams& p, const BBars& b, volatile int* abort_flag, uint32_t tmem, int bh,
+                            int i0, int nqb, int wq, int lane) {
+    using C = BCfg<D>;
+    const int row = wq * 32 + lane;
+    const uint32_t tQ = tmem + ((uint32_t)(wq * 32) << 16) + C::TM_S;
+    for (int it = 0; it < nqb; ++it) {
+        const bool okw = __all_sync(0xffffffffu, wait_bar(b.dq_full, (uint32_t)(it & 1), abort_flag, p.status));
+        if (!okw) return;
+        tc_fence_after();
+        float* acc = p.dq_acc + ((size_t)bh * p.nq_pad + (size_t)(i0 + it) * 128 + row) * D;
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t v[32];
+            tmem_ld32(tQ + 32 * ch, v);
+            tmem_ld_wait();
+            reg_after_wait<32>(v);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) red_add_v4(acc + 32 * ch + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+        tc_fence_before();
+        bar_arrive(b.dq_empty);
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
+    using C = BCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = blockIdx.x, bh = blockIdx.y;
+    const int i0 = first_qblock(p, j);
+    const int nqb = p.n_qblocks - i0 > 0 ? p.n_qblocks - i0 : 0;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    BBars b;
+    b.kv_full = bars;
+    b.qd_full = bars + 1;
+    b.qd_empty = bars + 3;
+    b.s_full = bars + 5;
+    b.ds_ready = bars + 6;
+    b.dq_full = bars + 7;
+    b.dq_empty = bars + 8;
+    b.done = bars + 9;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+    volatile int* skip = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+
+    if (threadIdx.x == 0) *skip = (*(volatile unsigned*)p.status != 0u) ? 1 : 0;
+    __syncthreads();
+    if (*skip) return;  // an earlier launch gave up: leave the device quiet
+
+    if (threadIdx.x == 0) {
+        bar_init(b.kv_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            bar_init(&b.qd_full[s], 1);
+            bar_init(&b.qd_empty[s], 1);
+        }
+        bar_init(b.s_full, 1);
+        bar_init(b.ds_ready, 128);
+        bar_init(b.dq_full, 1);
+        bar_init(b.dq_empty, 128);
+        bar_init(b.done, 1);
+        *abort_flag = 0;
+        bar_init_fence();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_holder, C::TM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp >= 2 && warp < 6) {
+        bwd_ds_role<D>(p, smem, b, abort_flag, tmem, bh, j, i0, nqb, warp & 3, lane);
+    } else if (warp >= 6) {
+        bwd_dq_role<D>(p, b, abort_flag, tmem, bh, i0, nqb, warp & 3, lane);
+    } else if (warp == 1) {
+        if (lane == 0 && nqb > 0) {
+            bwd_mma<D>(p, smem, b, abort_flag, tmem, nqb);
+            tc_commit(b.done);  // every issued MMA finishes before tensor memory is released
+            drain_wait(b.done, 0, p.status);
+        }
+        __syncwarp();
+    } else {
+        if (lane == 0 && nqb > 0) bwd_producer<D>(p, smem, b, abort_flag, bh, j, i0, nqb);
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, cudaStream_t stream) {
+    using C = BCfg<D>;
+    const long long prep_warps = (long long)p.BH * p.nq_pad;
+    bwd_prep_kernel<D><<<(unsigned)((prep_warps + 7) / 8), 256, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    bwd_main_kernel<D><<<dim3((unsigned)p.n_kblocks, (unsigned)p.BH), kBwdThreads, C::SMEM_BYTES, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long dq_warps = (long long)p.BH * p.Nq;
+    bwd_dq_kernel<D><<<(unsigned)((dq_warps + 7) / 8), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int BH, int Nq, int d) {
+    const size_t nq_pad = ((size_t)Nq + 127) / 128 * 128;
+    return (size_t)BH * nq_pad * ((size_t)d + 2) * sizeof(float);
+}
+
+cudaError_t launch_bwd(int d, const BwdParams& p, cudaStream_t stream) {
+    if (d == 128) return launch_bwd_d<128>(p, stream);
+    if (d == 64) return launch_bwd_d<64>(p, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

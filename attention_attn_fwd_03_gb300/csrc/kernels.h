@@ -105,6 +105,33 @@ PagedPlan paged_plan(int total_q, int max_q_len, int B, int H, int H_kv, int d, 
 int paged_smem_bytes(int d);
 cudaError_t launch_paged(int d, const PagedParams& p, int grid, cudaStream_t stream);
 
+// Backward: gradients of dense attention by recomputation from the LSE.
+struct BwdParams {
+    CUtensorMap tm_q;   // bf16 [BH, Nq, d], operand boxes as for prefill
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+    CUtensorMap tm_do;  // dO, like q
+    const uint16_t* o;     // bf16 [BH, Nq, d] forward output
+    const uint16_t* dout;  // bf16 [BH, Nq, d]
+    const float* lse;      // [BH, Nq] natural-log LSE from the forward pass
+    float* lse2;           // [BH, nq_pad] lse * log2(e), +inf where no key is visible / padding
+    float* dvec;           // [BH, nq_pad] rowsum(dO * O)
+    float* dq_acc;         // [BH, nq_pad, d] fp32 dQ accumulator (unscaled)
+    uint16_t* dq;          // bf16 [BH, Nq, d]
+    uint16_t* dk;          // bf16 [BH, Nk, d]
+    uint16_t* dv;          // bf16 [BH, Nk, d]
+    unsigned* status;
+    int BH, Nq, Nk, causal;
+    int n_qblocks, n_kblocks, nq_pad;
+    float c_scale;  // scale * log2(e)
+    float scale;
+};
+
+constexpr int kBwdThreads = 320;  // TMA warp, MMA warp, dS warpgroup, dQ warpgroup
+
+size_t bwd_workspace_bytes(int BH, int Nq, int d);
+cudaError_t launch_bwd(int d, const BwdParams& p, cudaStream_t stream);
+
 }  // namespace attn
 
 #include "attn.h"

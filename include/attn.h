@@ -219,6 +219,31 @@ attn_status_t attn_varlen_fwd(const void* q, const void* k, const void* v, const
                               int max_k_len, int H, int H_kv, int d, float scale, int causal, void* o,
                               float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace attn_bwd needs (0 on invalid sizes): an fp32 dQ
+ * accumulator and two fp32 row vectors, padded to whole 128-row blocks. */
+size_t attn_bwd_workspace_size(int B, int H, int Nq, int d);
+
+/* Backward pass of attn_fwd: dQ, dK, dV of O = softmax(scale Q K^T) V for
+ * the upstream gradient dO, recomputing the probabilities from Q, K and the
+ * forward pass's LSE instead of storing them ("Capstone" page, section 6.1,
+ * the pitfalls table: keep m, l and recompute; section 7.3, question 1):
+ *   P = exp(scale Q K^T - lse),  D = rowsum(dO * O),  dS = P * (dO V^T - D),
+ *   dV = P^T dO,  dQ = scale dS K,  dK = scale dS^T Q.
+ *   q, o, dout: bf16 [B, H, Nq, d]; k, v: bf16 [B, H, Nk, d]; lse: fp32
+ *   [B, H, Nq], all as produced / consumed by attn_fwd with the same scale
+ *   and causal flag (read only); dq: bf16 [B, H, Nq, d], dk, dv: bf16
+ *   [B, H, Nk, d] (written).  P and dS enter the tensor-core products as
+ *   bf16, accumulation is fp32, dQ is accumulated across key blocks in fp32
+ *   and rounded once.  Rows with lse = -inf (no visible key) get dQ = 0;
+ *   keys no query sees get dK = dV = 0.
+ *   workspace: attn_bwd_workspace_size(B, H, Nq, d) bytes, caller-owned,
+ *   16-byte aligned, no initialisation needed.
+ *   d in {64, 128}; B * H <= 65535.  Errors as attn_fwd, plus
+ *   ATTN_ERR_WORKSPACE. */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                       float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, then reads and clears the calling device's status
  * word.  Kernels set it when a bounded internal wait gives up
  * (ATTN_ERR_TIMEOUT; the kernel then returns early and its outputs are

@@ -3,6 +3,7 @@
 Tolerances (max abs error against the float64 oracle on the same inputs):
   bf16 prefill and paged decode: O <= 2e-2, LSE <= 1e-3
   FP8 prefill: O <= 6e-2 (oracle on the dequantised inputs), LSE <= 1e-3
+  backward: max error <= 2e-2 of the gradient tensor's largest entry
 Rows with no visible key must come back as O = 0 and LSE = -inf exactly.
 """
 import json
@@ -14,6 +15,23 @@ import numpy as np
 TOL_O_BF16 = 2e-2
 TOL_LSE = 1e-3
 TOL_O_FP8 = 6e-2
+# backward: max |g - oracle| relative to max |oracle| per gradient tensor.  P
+# and dS enter the products as bf16 (relative rounding 2^-9 per element) and
+# D uses the bf16 forward output; summed over up to Nk terms of random sign
+# the error stays well below 1% of the tensor's largest entry, while an index
+# or sign mistake gives errors of order 1.
+TOL_GRAD_REL = 2e-2
+
+
+def compare_grad(name, g_gpu, g_ref, tol_rel=TOL_GRAD_REL):
+    g = g_gpu.float().cpu().numpy().astype(np.float64).reshape(g_ref.shape)
+    assert np.all(np.isfinite(g)), name + ": non-finite gradient"
+    scale = float(np.max(np.abs(g_ref))) if g_ref.size else 0.0
+    err = float(np.max(np.abs(g - g_ref))) if g.size else 0.0
+    rel = err / scale if scale > 0 else err
+    record(name, rel, 0.0, g.shape)
+    assert rel <= tol_rel, "%s: max |g - oracle| / max |oracle| = %.3g > %.3g" % (name, rel, tol_rel)
+    return rel
 
 
 def f32(x):

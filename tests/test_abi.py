@@ -29,6 +29,7 @@ def test_header_declares_the_entry_points():
                                   "attn_paged_decode_workspace_size", "attn_paged_decode_noalloc",
                                   "attn_paged_fwd", "attn_paged_fwd_workspace_size",
                                   "attn_varlen_fwd", "attn_varlen_fwd_workspace_size",
+                                  "attn_bwd", "attn_bwd_workspace_size",
                                   "attn_device_status", "attn_status_string"])
 
 
@@ -164,3 +165,16 @@ def test_varlen_fwd_validation(L):
     assert attn.attn_varlen_fwd(**dict(base, d=80)) == attn.ATTN_ERR_UNSUPPORTED
     assert attn.attn_varlen_fwd(**dict(base, workspace_bytes=ws - 1)) == attn.ATTN_ERR_WORKSPACE
     assert attn.attn_varlen_fwd(**dict(base, cu_seqlens_q=FAKE + 2)) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_bwd_validation(L):
+    ws = attn.attn_bwd_workspace_size(2, 4, 300, 128)
+    assert ws == 2 * 4 * 384 * 130 * 4  # dQ accumulator + two row vectors, rows padded to 128
+    assert attn.attn_bwd_workspace_size(2, 4, 300, 96) == 0
+    base = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, dout=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=2, H=4, Nq=300,
+                Nk=300, d=128, scale=0.088, causal=1, workspace=FAKE, workspace_bytes=ws, stream=None)
+    assert attn.attn_bwd(**dict(base, lse=None)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_bwd(**dict(base, dk=FAKE + 8)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_bwd(**dict(base, d=96)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_bwd(**dict(base, workspace_bytes=ws - 4)) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_bwd(**dict(base, causal=3)) == attn.ATTN_ERR_INVALID_ARG
