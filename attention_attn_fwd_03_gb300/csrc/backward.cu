@@ -24,11 +24,13 @@
 //                             dV += P^T dO_i, dK += dS^T Q_i       (A = P^T / dS^T from TMEM)
 //                             dQ_i = dS K_j                       (A = dS from shared memory)
 //                 warps 2-5 one thread per key: P^T and dS^T from S^T, dP^T, lse2, D
-//                           (masked pairs: 0); P^T, dS^T back to TMEM as bf16 and dS to
+//                           (the block's lse2 and D staged in shared memory, one entry
+//                           per thread; masked pairs: 0); P^T, dS^T back to TMEM as bf16 and dS to
 //                           shared memory in the layout the dQ product reads;
 //                           at the end dK (times scale) and dV -> bf16 -> global
-//                 warps 6-9 one thread per query: dQ_i from TMEM added into the fp32
-//                           accumulator with vector reductions (red.global.add.v4.f32)
+//                 warps 6-9 one thread per query: dQ_i from TMEM to registers (TMEM
+//                           released at once), then added into the fp32 accumulator
+//                           with vector reductions (red.global.add.v4.f32)
 //   bwd_dq      dQ = scale * accumulator -> bf16.
 //
 // Tensor memory: columns 0-127 S^T, then P^T over it, then dQ_i; 128-255
@@ -58,7 +60,8 @@ struct BCfg {
     static constexpr int OFF_Q = OFF_V + TILE_BYTES;        // [2]
     static constexpr int OFF_DO = OFF_Q + 2 * TILE_BYTES;   // [2]
     static constexpr int OFF_DS = OFF_DO + 2 * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+    static constexpr int OFF_LD = OFF_DS + DS_BYTES;        // lse2[128], D[128] of the current query block
+    static constexpr int OFF_BAR = OFF_LD + 2 * 128 * 4;
     static constexpr int N_BARS = 12;
     static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
     static constexpr int SMEM_USED = OFF_MISC + 16;
@@ -77,6 +80,8 @@ struct BBars {
     uint64_t* dq_full;   // dQ_i computed (also: dS in shared memory consumed)
     uint64_t* dq_empty;  // 128 arrivals: dQ_i read out of TMEM
     uint64_t* done;      // all products finished (dK, dV final)
+    uint64_t* ld_full;   // 128 arrivals: lse2 / D of the block staged in shared memory
+    uint64_t* ld_free;   // 128 arrivals: every dS thread has finished reading them
 };
 
 // Query blocks a key block j sees: [i0, n_qb).  Under the causal mask query
@@ -239,9 +244,30 @@ __device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, v
     const int off = p.Nk - p.Nq;
     const float cs = p.c_scale;
     const uint32_t ds_row = smem_u32(smem + C::OFF_DS) + (uint32_t)(row * 128);
+    float* lds = reinterpret_cast<float*>(smem + C::OFF_LD);  // [0, 128): lse2, [128, 256): D
+    // this thread's lse2 / D entry of the next query block, loaded one block ahead
+    const float* l2g = p.lse2 + (size_t)bh * p.nq_pad + (size_t)i0 * 128 + row;
+    const float* dvg = p.dvec + (size_t)bh * p.nq_pad + (size_t)i0 * 128 + row;
+    float nx_l = nqb > 0 ? l2g[0] : 0.f, nx_d = nqb > 0 ? dvg[0] : 0.f;
     bool ok = true;
     for (int it = 0; ok && it < nqb; ++it) {
         const int i = i0 + it;
+        // stage the block's lse2 and D once every thread is done with the
+        // previous block's, then start loading the following block's
+        const float my_l = nx_l, my_d = nx_d;
+        if (it + 1 < nqb) {
+            nx_l = l2g[(size_t)(it + 1) * 128];
+            nx_d = dvg[(size_t)(it + 1) * 128];
+        }
+        if (it > 0) {
+            ok = __all_sync(0xffffffffu, wait_bar(b.ld_free, (uint32_t)((it - 1) & 1), abort_flag, p.status));
+            if (!ok) break;
+        }
+        lds[row] = my_l;
+        lds[128 + row] = my_d;
+        bar_arrive(b.ld_full);
+        ok = __all_sync(0xffffffffu, wait_bar(b.ld_full, (uint32_t)(it & 1), abort_flag, p.status));
+        if (!ok) break;
         ok = __all_sync(0xffffffffu, wait_bar(b.s_full, (uint32_t)(it & 1), abort_flag, p.status));
         if (!ok) break;
         // dS in shared memory is free once the previous block's dQ product read it
@@ -252,8 +278,8 @@ __device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, v
         tc_fence_after();
         // first query of the block that sees this key (earlier queries are masked)
         const long long q_min = (long long)key - off;
-        const float* l2 = p.lse2 + ((size_t)bh * p.nq_pad + (size_t)i * 128);
-        const float* dv = p.dvec + ((size_t)bh * p.nq_pad + (size_t)i * 128);
+        const float* l2 = lds;
+        const float* dv = lds + 128;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {  // 32 queries per chunk
             uint32_t sv[32], dp[32];
@@ -298,6 +324,7 @@ __device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, v
         fence_async_smem();
         tc_fence_before();
         bar_arrive(b.ds_ready);
+        bar_arrive(b.ld_free);
     }
     if (!ok) return;
     // ---- epilogue: dV and scale * dK rows of this key block -> bf16
@@ -351,18 +378,18 @@ __device__ void bwd_dq_role(const BwdParams& p, const BBars& b, volatile int* ab
         const bool okw = __all_sync(0xffffffffu, wait_bar(b.dq_full, (uint32_t)(it & 1), abort_flag, p.status));
         if (!okw) return;
         tc_fence_after();
-        float* acc = p.dq_acc + ((size_t)bh * p.nq_pad + (size_t)(i0 + it) * 128 + row) * D;
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t v[32];
-            tmem_ld32(tQ + 32 * ch, v);
-            tmem_ld_wait();
-            reg_after_wait<32>(v);
+        // the whole row into registers first: TMEM is released before the
+        // reductions, which then overlap the next block's products
+        uint32_t v[D];
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) red_add_v4(acc + 32 * ch + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
-        }
+        for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tQ + 32 * ch, v + 32 * ch);
+        tmem_ld_wait();
+        reg_after_wait<D>(v);
         tc_fence_before();
         bar_arrive(b.dq_empty);
+        float* acc = p.dq_acc + ((size_t)bh * p.nq_pad + (size_t)(i0 + it) * 128 + row) * D;
+#pragma unroll
+        for (int e = 0; e < D; e += 4) red_add_v4(acc + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
     }
 }
 
@@ -386,6 +413,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     b.dq_full = bars + 7;
     b.dq_empty = bars + 8;
     b.done = bars + 9;
+    b.ld_full = bars + 10;
+    b.ld_free = bars + 11;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     volatile int* skip = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -405,6 +434,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         bar_init(b.dq_full, 1);
         bar_init(b.dq_empty, 128);
         bar_init(b.done, 1);
+        bar_init(b.ld_full, 128);
+        bar_init(b.ld_free, 128);
         *abort_flag = 0;
         bar_init_fence();
     }

@@ -16,7 +16,8 @@ cores -- both as HBM GB/s of algorithmic bytes -- and causal prefill chunks
 over a paged cache (8 requests x 2048 new tokens after 6144 cached, 32 query
 heads over 8 KV heads) and a variable-length causal batch (16 packed sequences of 512..4096
 tokens, 32 query heads over 8 KV heads) as TFLOPS of exactly counted
-visible pairs.
+visible pairs; and the backward pass of the batched workload (dQ, dK, dV),
+as TFLOPS with 2.5x the forward count.
 
 `--impl reference` times the float64 CPU oracle (the only reference this
 method has) on a bounded row sample of the same workload.
@@ -484,6 +485,28 @@ def run_secondary(torch, attn, inputs, dev, flush, peaks, rank):
         "flops_note": "4 * d * H * visible (query, key) pairs, counted exactly"}
     del p, o, l, ws
     torch.cuda.empty_cache()
+    # backward of the batched prefill (4 x 16 x 2048, d = 128): dQ, dK, dV by recomputation
+    q, k, v = (t.to(dev) for t in inputs.dense_qkv(B, H, N, N, D, seed=rank))
+    g = torch.Generator(device="cpu").manual_seed(rank + 1)
+    do = torch.randn((B, H, N, D), generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
+    ws = torch.empty(attn.attn_bwd_workspace_size(B, H, N, D), dtype=torch.uint8, device=dev)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    for causal in (False, True):
+        o, l = attn.fwd(q, k, v, causal=causal)
+
+        def bwd():
+            attn.bwd(q, k, v, o, l, do, causal=causal, dq=grads[0], dk=grads[1], dv=grads[2], workspace=ws)
+        bwd()
+        ms = timed_launches(torch, bwd, reps, flush)
+        attn.device_status()
+        f = 2.5 * prefill_flops(B, H, N, N, D, causal)  # five products of the forward's size
+        tf = f / (statistics.mean(ms) * 1e-3) / 1e12
+        out["backward_%dx%dx%d_d%d_%s" % (B, H, N, D, "causal" if causal else "non_causal")] = {
+            "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
+            "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4),
+            "flops_note": "2.5 x the forward count (five GEMMs of the forward's size), halved for causal"}
+    del q, k, v, do, ws, grads, o, l
+    torch.cuda.empty_cache()
     return out
 
 
@@ -601,6 +624,11 @@ def run_profile_case(args):
         p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
                             len_hi=8192, seed=0, device=dev, H_kv=8)
         fns = [lambda: attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"])]
+    elif case == "bwd_small":
+        q, k, v = (t.to(dev) for t in inputs.dense_qkv(1, 8, 2048, 2048, 128, seed=0))
+        do = torch.randn((1, 8, 2048, 128), generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).to(dev)
+        o, lse = attn.fwd(q, k, v, causal=True)
+        fns = [lambda: attn.bwd(q, k, v, o, lse, do, causal=True)]
     elif case == "chunks_small":
         p = inputs.paged_chunks(B=2, H=32, H_kv=8, d=128, page_size=64, max_pages=128, num_pages=256,
                                 q_lo=2048, q_hi=2048, ctx_lo=6144, ctx_hi=6144, seed=0, device=dev)
@@ -634,7 +662,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["step", "long_small", "fp8", "decode_small", "gqa_decode_small",
-                                               "gqa_decode", "chunks_small"], default=None,
+                                               "gqa_decode", "chunks_small", "bwd_small"], default=None,
                     help="run one small workload for an ncu capture instead of the benchmark")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
