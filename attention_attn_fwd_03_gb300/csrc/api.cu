@@ -415,6 +415,16 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     const int nq_pad = (Nq + 127) / 128 * 128;
     char* ws = static_cast<char*>(workspace);
     p.dq_acc = reinterpret_cast<float*>(ws);
+    {  // reduce target of the dQ boxes: 32 fp32 columns x 32 rows, 128-byte swizzle
+        cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)nq_pad, (cuuint64_t)BH};
+        cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)nq_pad * d * 4};
+        cuuint32_t box[3] = {32u, 32u, 1u};
+        cuuint32_t estr[3] = {1u, 1u, 1u};
+        if (g_encode(&p.tm_dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.dq_acc, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return ATTN_ERR_CUDA;
+    }
     p.lse2 = reinterpret_cast<float*>(ws + (size_t)BH * nq_pad * d * sizeof(float));
     p.dvec = p.lse2 + (size_t)BH * nq_pad;
     p.o = static_cast<const uint16_t*>(o);

@@ -29,8 +29,9 @@
 //                           shared memory in the layout the dQ product reads;
 //                           at the end dK (times scale) and dV -> bf16 -> global
 //                 warps 6-9 one thread per query: dQ_i from TMEM to registers (TMEM
-//                           released at once), then added into the fp32 accumulator
-//                           with vector reductions (red.global.add.v4.f32)
+//                           released at once), staged in the block's own Q / dO slot
+//                           (free once the products reading it are done) and added
+//                           into the fp32 accumulator by bulk tensor reductions
 //   bwd_dq      dQ = scale * accumulator -> bf16.
 //
 // Tensor memory: columns 0-127 S^T, then P^T over it, then dQ_i; 128-255
@@ -67,6 +68,7 @@ struct BCfg {
     static constexpr int SMEM_USED = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = (SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024);
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(2 * (D / 32) * 4096 <= TILE_BYTES, "two warps' dQ staging fits one Q or dO slot");
     // dQ = dS K: A = dS (MN-major: queries contiguous), B = K_j (MN-major: dims contiguous)
     static constexpr uint32_t ID_DQ = idesc_make(128, D, 1u, true, true);
 };
@@ -74,7 +76,7 @@ struct BCfg {
 struct BBars {
     uint64_t* kv_full;
     uint64_t* qd_full;   // [2]
-    uint64_t* qd_empty;  // [2]
+    uint64_t* qd_empty;  // [2], the products reading Q_i / dO_i done (1) and dQ_i staged out of the slot (4)
     uint64_t* s_full;    // S^T and dP^T computed
     uint64_t* ds_ready;  // 128 arrivals: P^T, dS^T in TMEM, dS in shared memory
     uint64_t* dq_full;   // dQ_i computed (also: dS in shared memory consumed)
@@ -92,12 +94,6 @@ __device__ __forceinline__ int first_qblock(const BwdParams& p, int j) {
     const long long need = (long long)j * 128 - (p.Nk - p.Nq) - 127;  // smallest useful last-query index
     if (need <= 0) return 0;
     return (int)((need + 127) / 128);
-}
-
-__device__ __forceinline__ void red_add_v4(float* ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "f"(__uint_as_float(a)),
-                 "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
-                 : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -369,17 +365,20 @@ __device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, v
 // One thread per query row of the block (TMEM lane): dQ_i added into the
 // accumulator (padded rows, so every row of a block exists).
 template <int D>
-__device__ void bwd_dq_role(const BwdParams& p, const BBars& b, volatile int* abort_flag, uint32_t tmem, int bh,
-                            int i0, int nqb, int wq, int lane) {
+__device__ void bwd_dq_role(const BwdParams& p, uint8_t* smem, const BBars& b, volatile int* abort_flag,
+                            uint32_t tmem, int bh, int i0, int nqb, int wq, int lane) {
     using C = BCfg<D>;
-    const int row = wq * 32 + lane;
     const uint32_t tQ = tmem + ((uint32_t)(wq * 32) << 16) + C::TM_S;
+    if (lane == 0) tma_prefetch_map(&p.tm_dq);
+    // this warp's staging area: 32 rows x d fp32, in the Q slot (warps 0, 1) or
+    // the dO slot (warps 2, 3) of the block's buffer pair
+    const int stage_off = (wq < 2 ? C::OFF_Q : C::OFF_DO) + (wq & 1) * (D / 32) * 4096;
     for (int it = 0; it < nqb; ++it) {
+        const int s = it & 1;
         const bool okw = __all_sync(0xffffffffu, wait_bar(b.dq_full, (uint32_t)(it & 1), abort_flag, p.status));
-        if (!okw) return;
+        if (!okw) break;
         tc_fence_after();
-        // the whole row into registers first: TMEM is released before the
-        // reductions, which then overlap the next block's products
+        // the whole row into registers first: TMEM is released at once
         uint32_t v[D];
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tQ + 32 * ch, v + 32 * ch);
@@ -387,10 +386,35 @@ __device__ void bwd_dq_role(const BwdParams& p, const BBars& b, volatile int* ab
         reg_after_wait<D>(v);
         tc_fence_before();
         bar_arrive(b.dq_empty);
-        float* acc = p.dq_acc + ((size_t)bh * p.nq_pad + (size_t)(i0 + it) * 128 + row) * D;
+        // Stage the warp's 32 rows in the block's Q / dO slot (free: the products
+        // that read it completed before dQ_i) as D / 32 boxes of 32 rows x 32 fp32
+        // (128 B rows, 128-byte swizzle: 16-byte chunk k of row r at k ^ (r % 8)),
+        // then let the bulk-copy engine add them into the accumulator.
+        uint8_t* stage_p = smem + stage_off + s * C::TILE_BYTES;
+        const uint32_t stage = smem_u32(stage_p);
 #pragma unroll
-        for (int e = 0; e < D; e += 4) red_add_v4(acc + e, v[e], v[e + 1], v[e + 2], v[e + 3]);
+        for (int ch = 0; ch < D / 32; ++ch) {
+            const uint32_t rowp = stage + (uint32_t)(ch * 4096 + lane * 128);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                st_shared_v4(rowp + (((uint32_t)k ^ (uint32_t)(lane & 7)) << 4), v[32 * ch + 4 * k],
+                             v[32 * ch + 4 * k + 1], v[32 * ch + 4 * k + 2], v[32 * ch + 4 * k + 3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            const int row0 = (i0 + it) * 128 + wq * 32;
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch)
+                tma_reduce_add_3d(&p.tm_dq, stage_p + ch * 4096, ch * 32, row0, bh);
+            tma_store_commit();
+            tma_wait_read_all();  // the slot may be refilled once the engine has read it
+            bar_arrive(&b.qd_empty[s]);
+        }
+        __syncwarp();
     }
+    if (lane == 0) tma_store_wait_all();  // every reduction has landed before the CTA exits
+    __syncwarp();
 }
 
 template <int D>
@@ -427,7 +451,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
         bar_init(b.kv_full, 1);
         for (int s = 0; s < 2; ++s) {
             bar_init(&b.qd_full[s], 1);
-            bar_init(&b.qd_empty[s], 1);
+            bar_init(&b.qd_empty[s], 5);
         }
         bar_init(b.s_full, 1);
         bar_init(b.ds_ready, 128);
@@ -451,7 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     if (warp >= 2 && warp < 6) {
         bwd_ds_role<D>(p, smem, b, abort_flag, tmem, bh, j, i0, nqb, warp & 3, lane);
     } else if (warp >= 6) {
-        bwd_dq_role<D>(p, b, abort_flag, tmem, bh, i0, nqb, warp & 3, lane);
+        bwd_dq_role<D>(p, smem, b, abort_flag, tmem, bh, i0, nqb, warp & 3, lane);
     } else if (warp == 1) {
         if (lane == 0 && nqb > 0) {
             bwd_mma<D>(p, smem, b, abort_flag, tmem, nqb);

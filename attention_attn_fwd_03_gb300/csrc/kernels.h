@@ -111,6 +111,7 @@ struct BwdParams {
     CUtensorMap tm_k;
     CUtensorMap tm_v;
     CUtensorMap tm_do;  // dO, like q
+    CUtensorMap tm_dq;  // fp32 dQ accumulator [BH, nq_pad, d]: box (32, 32, 1), 128-byte swizzle
     const uint16_t* o;     // bf16 [BH, Nq, d] forward output
     const uint16_t* dout;  // bf16 [BH, Nq, d]
     const float* lse;      // [BH, Nq] natural-log LSE from the forward pass
