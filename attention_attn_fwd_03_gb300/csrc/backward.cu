@@ -240,7 +240,7 @@ __device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, v
     const int off = p.Nk - p.Nq;
     const float cs = p.c_scale;
     const uint32_t ds_row = smem_u32(smem + C::OFF_DS) + (uint32_t)(row * 128);
-    float* lds = reinterpret_cast<float*>(smem + C::OFF_LD);  // [0, 128): lse2, [128, 256): D
+    float* lds = reinterpret_cast<float*>(smem + C::OFF_LD);  // [0, 128): -lse2, [128, 256): -D
     // this thread's lse2 / D entry of the next query block, loaded one block ahead
     const float* l2g = p.lse2 + (size_t)bh * p.nq_pad + (size_t)i0 * 128 + row;
     const float* dvg = p.dvec + (size_t)bh * p.nq_pad + (size_t)i0 * 128 + row;
@@ -259,8 +259,8 @@ __device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, v
             ok = __all_sync(0xffffffffu, wait_bar(b.ld_free, (uint32_t)((it - 1) & 1), abort_flag, p.status));
             if (!ok) break;
         }
-        lds[row] = my_l;
-        lds[128 + row] = my_d;
+        lds[row] = -my_l;  // stored negated: the score step is one fma, the dS step one add
+        lds[128 + row] = -my_d;
         bar_arrive(b.ld_full);
         ok = __all_sync(0xffffffffu, wait_bar(b.ld_full, (uint32_t)(it & 1), abort_flag, p.status));
         if (!ok) break;
@@ -272,10 +272,14 @@ __device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, v
             if (!ok) break;
         }
         tc_fence_after();
-        // first query of the block that sees this key (earlier queries are masked)
-        const long long q_min = (long long)key - off;
-        const float* l2 = lds;
-        const float* dv = lds + 128;
+        // Queries of this block before `vis_from` do not see this key (causal
+        // mask); the whole warp takes the mask-free path when none of its keys
+        // needs it.  Scores, shifts and products run as packed pairs.
+        const int vis_from = key_ok ? (p.causal ? key - off - i * 128 : 0) : 128;
+        const bool all_visible = __all_sync(0xffffffffu, vis_from <= 0);
+        const float* nl = lds;        // -lse2 of the block's queries
+        const float* nd = lds + 128;  // -D
+        const uint64_t cs2 = f2_pack(cs, cs);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {  // 32 queries per chunk
             uint32_t sv[32], dp[32];
@@ -287,23 +291,30 @@ __device__ void bwd_ds_role(const BwdParams& p, uint8_t* smem, const BBars& b, v
             uint32_t pw[16], dw[16];
 #pragma unroll
             for (int t4 = 0; t4 < 8; ++t4) {
-                const float4 L = *reinterpret_cast<const float4*>(l2 + 32 * c + 4 * t4);
-                const float4 Dv = *reinterpret_cast<const float4*>(dv + 32 * c + 4 * t4);
-                const float Ls[4] = {L.x, L.y, L.z, L.w};
-                const float Ds[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
-                float pv[4], ds[4];
+                const float4 L = *reinterpret_cast<const float4*>(nl + 32 * c + 4 * t4);
+                const float4 Dn = *reinterpret_cast<const float4*>(nd + 32 * c + 4 * t4);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int t = 4 * t4 + e;
-                    const long long q = (long long)i * 128 + 32 * c + t;
-                    const bool vis = key_ok && (!p.causal || q >= q_min);
-                    pv[e] = vis ? ex2(fmaf(__uint_as_float(sv[t]), cs, -Ls[e])) : 0.f;
-                    ds[e] = pv[e] * (__uint_as_float(dp[t]) - Ds[e]);
+                for (int h = 0; h < 2; ++h) {
+                    const int t = 4 * t4 + 2 * h;
+                    const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), cs2,
+                                              h ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y));
+                    float p0, p1;
+                    f2_unpack(x, p0, p1);
+                    p0 = ex2(p0);
+                    p1 = ex2(p1);
+                    if (!all_visible) {
+                        const int tq = 32 * c + t;  // query index within the block
+                        p0 = tq >= vis_from ? p0 : 0.f;
+                        p1 = tq + 1 >= vis_from ? p1 : 0.f;
+                    }
+                    const uint64_t pp = f2_pack(p0, p1);
+                    const uint64_t diff = f2_add(f2_pack(__uint_as_float(dp[t]), __uint_as_float(dp[t + 1])),
+                                                 h ? f2_pack(Dn.z, Dn.w) : f2_pack(Dn.x, Dn.y));
+                    float d0, d1;
+                    f2_unpack(f2_mul(pp, diff), d0, d1);
+                    pw[2 * t4 + h] = pack_bf16(p0, p1);
+                    dw[2 * t4 + h] = pack_bf16(d0, d1);
                 }
-                pw[2 * t4] = pack_bf16(pv[0], pv[1]);
-                pw[2 * t4 + 1] = pack_bf16(pv[2], pv[3]);
-                dw[2 * t4] = pack_bf16(ds[0], ds[1]);
-                dw[2 * t4 + 1] = pack_bf16(ds[2], ds[3]);
             }
             tmem_st16(tS + 16 * c, pw);
             tmem_st16(tP + 16 * c, dw);
