@@ -482,10 +482,12 @@ __device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b
             reg_after_wait<128>(s);
 
             const long long kbase = (long long)(g.kb0 + j) * 128;
-            if (kbase + 127 > tile_limit) {
+            if (kbase + 127 > tile_limit) {  // visible columns of this row: [0, bound)
+                const long long bl = limit - kbase + 1;
+                const int bound = bl < 0 ? 0 : (bl > 128 ? 128 : (int)bl);
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
-                    if (kbase + c > limit) s[c] = __float_as_uint(-INFINITY);
+                    if (c >= bound) s[c] = __float_as_uint(-INFINITY);
             }
             float mc[8];
 #pragma unroll

@@ -366,11 +366,15 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
             const bool need_mask =
                 (kbase + 128 > p.Nk) || (p.causal && (long long)kbase + 127 > (long long)q0 + off);
             if (need_mask) {
+                // visible columns of this row: [0, bound), the keys up to
+                // min(Nk - 1, limit) (causal) or Nk - 1
+                long long last = (long long)p.Nk - 1;
+                if (p.causal && limit < last) last = limit;
+                long long bl = last - kbase + 1;
+                const int bound = bl < 0 ? 0 : (bl > 128 ? 128 : (int)bl);
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = kbase + c;
-                    if (key >= p.Nk || (p.causal && (long long)key > limit)) s[c] = __float_as_uint(-INFINITY);
-                }
+                for (int c = 0; c < 128; ++c)
+                    if (c >= bound) s[c] = __float_as_uint(-INFINITY);
             }
             // row max: eight independent chains of 3-input max
             float mc[8];
