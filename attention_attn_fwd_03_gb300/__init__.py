@@ -9,14 +9,14 @@ Two levels:
     ``attn_paged_decode_workspace_size``, ``attn_paged_decode_noalloc``,
     ``attn_paged_fwd``, ``attn_paged_fwd_workspace_size``,
     ``attn_varlen_fwd``, ``attn_varlen_fwd_workspace_size``, ``attn_bwd``,
-    ``attn_bwd_workspace_size``,
+    ``attn_bwd_workspace_size``, ``attn_fwd_host``, ``attn_fwd_host_workspace_size``,
     ``attn_device_status``, ``attn_status_string``: the C entry points, same
     names and argument order, taking raw device pointers (ints) and a stream
     handle (int).
   * ``fwd``, ``fwd_fp8``, ``paged_decode``, ``paged_fwd``, ``varlen_fwd``, ``bwd``: take torch CUDA
-    tensors, allocate
-    outputs with torch when none are given, call the C entry point on the
-    current stream and raise ``AttnError`` on a non-zero status.
+    tensors, allocate outputs with torch when none are given, call the C entry
+    point on the current stream and raise ``AttnError`` on a non-zero status.
+  * ``fwd_host``: the same for host (CPU) tensors through ``attn_fwd_host``.
 """
 import ctypes
 import math
@@ -89,6 +89,10 @@ def lib():
             L.attn_bwd_workspace_size.argtypes = [i, i, i, i]
             L.attn_bwd.restype = i
             L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+            L.attn_fwd_host_workspace_size.restype = sz
+            L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.attn_fwd_host.restype = i
+            L.attn_fwd_host.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
             L.attn_device_status.restype = i
             L.attn_device_status.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -159,6 +163,17 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, 
                           workspace_bytes, stream)
 
 
+def attn_fwd_host_workspace_size(B, H, Nq, Nk, d, n_modes, chunk_bh):
+    return lib().attn_fwd_host_workspace_size(B, H, Nq, Nk, d, n_modes, chunk_bh)
+
+
+def attn_fwd_host(q, k, v, n_modes, causal, o, lse, B, H, Nq, Nk, d, scale, chunk_bh, workspace, workspace_bytes,
+                  stream):
+    """causal, o and lse are addresses of C arrays of n_modes entries (int, pointer, pointer)."""
+    return lib().attn_fwd_host(q, k, v, n_modes, causal, o, lse, B, H, Nq, Nk, d, scale, chunk_bh, workspace,
+                               workspace_bytes, stream)
+
+
 def attn_device_status(stream):
     return lib().attn_device_status(stream)
 
@@ -192,6 +207,18 @@ def _check(t, name, dtype, shape=None):
         raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
 
 
+def _check_host(t, name, dtype, shape=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError("%s must be a CPU (host) tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
 def _raise(st, what):
     if st != ATTN_OK:
         raise AttnError(st, what)
@@ -217,6 +244,51 @@ def fwd(q, k, v, causal=False, scale=None, out=None, lse=None, return_lse=True, 
                   lse.data_ptr() if lse is not None else None, B, H, Nq, Nk, d, sc, int(bool(causal)),
                   _stream(stream))
     _raise(st, "attn_fwd")
+    return out, lse
+
+
+def fwd_host(q, k, v, causal=(False,), scale=None, out=None, lse=None, chunk_bh=0, workspace=None, stream=None,
+             synchronize=True):
+    """Host-resident bf16 q [B,H,Nq,d], k, v [B,H,Nk,d] -> (list of o, list of lse), one entry per mask mode
+    in ``causal``.  Outputs are page-locked host tensors unless given.  The copies and kernels run on the
+    library's chunk pipeline.  With ``synchronize`` (the default) the call returns after synchronising the
+    stream, so the outputs are ready; otherwise they are ready once the stream reaches this point."""
+    torch = _torch()
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    _check_host(q, "q", torch.bfloat16)
+    _check_host(k, "k", torch.bfloat16, (B, H, Nk, d))
+    _check_host(v, "v", torch.bfloat16, (B, H, Nk, d))
+    modes = [int(bool(c)) for c in causal]
+    n = len(modes)
+    if out is None:
+        out = [torch.empty(q.shape, dtype=torch.bfloat16).pin_memory() for _ in range(n)]
+    if lse is None:
+        lse = [torch.empty((B, H, Nq), dtype=torch.float32).pin_memory() for _ in range(n)]
+    if len(out) != n or len(lse) != n:
+        raise ValueError("need one out and one lse per mode")
+    for m in range(n):
+        _check_host(out[m], "out[%d]" % m, torch.bfloat16, q.shape)
+        if lse[m] is not None:
+            _check_host(lse[m], "lse[%d]" % m, torch.float32, (B, H, Nq))
+    need = attn_fwd_host_workspace_size(B, H, Nq, Nk, d, n, chunk_bh)
+    if need == 0:
+        raise AttnError(ATTN_ERR_INVALID_ARG, "attn_fwd_host_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    if workspace.device.type != "cuda" or workspace.numel() < need:
+        raise ValueError("workspace must be a CUDA tensor of at least %d bytes" % need)
+    c_modes = (ctypes.c_int * n)(*modes)
+    c_out = (ctypes.c_void_p * n)(*[t.data_ptr() for t in out])
+    c_lse = (ctypes.c_void_p * n)(*[(t.data_ptr() if t is not None else None) for t in lse])
+    sc = float(scale) if scale is not None else 1.0 / math.sqrt(d)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), n, ctypes.addressof(c_modes),
+                       ctypes.addressof(c_out), ctypes.addressof(c_lse), B, H, Nq, Nk, d, sc, int(chunk_bh),
+                       workspace.data_ptr(), workspace.numel(), s.cuda_stream)
+    _raise(st, "attn_fwd_host")
+    if synchronize:
+        s.synchronize()
     return out, lse
 
 

@@ -2,8 +2,9 @@
 //
 // Host-side only: argument validation (nothing is enqueued on a bad
 // argument), TMA tensor-map encoding, per-device cached state (the device
-// status word's address), and the kernel launches.  No allocation happens
-// here or in any kernel.
+// status word's address), the kernel launches, and the chunked copy/compute
+// pipeline of attn_fwd_host (two streams and ten events per device, created
+// on its first call).  No memory is allocated here or in any kernel.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -153,6 +154,103 @@ bool make_paged_map(CUtensorMap* map, const void* base, int d, long long heads, 
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// ---- host-staged prefill: copy in, compute, copy out, chunk by chunk.
+//
+// The (b, h) range is cut into chunks.  Chunk c uses workspace slot
+// c % kHostSlots: its Q/K/V are copied in on stream s_in, its kernels run on
+// the caller's stream, its O/LSE are copied out on stream s_out.  Events per
+// slot order the three stages and the reuse of a slot three chunks later:
+//   copy-in of c    after the kernels of c - kHostSlots (comp_done)
+//   kernels of c    after copy-in of c (in_done) and copy-out of c - kHostSlots (out_done)
+//   copy-out of c   after the kernels of c (comp_done)
+constexpr int kHostSlots = 3;
+constexpr int kHostMaxModes = 8;
+
+struct HostStage {
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t entry = nullptr;
+    cudaEvent_t in_done[kHostSlots] = {}, comp_done[kHostSlots] = {}, out_done[kHostSlots] = {};
+};
+
+std::mutex g_host_mu;
+HostStage g_host[kMaxDevices];
+
+size_t round_up256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Byte sizes of the buffers in one slot (each rounded up to 256 bytes).
+struct SlotLayout {
+    size_t q, kv, o, lse, per_mode, slot;
+};
+
+SlotLayout slot_layout(long long cb, int Nq, int Nk, int d, int n_modes) {
+    SlotLayout L;
+    L.q = round_up256((size_t)cb * Nq * d * 2);
+    L.kv = round_up256((size_t)cb * Nk * d * 2);
+    L.o = L.q;
+    L.lse = round_up256((size_t)cb * Nq * 4);
+    L.per_mode = L.o + L.lse;
+    L.slot = L.q + 2 * L.kv + (size_t)n_modes * L.per_mode;
+    return L;
+}
+
+// Pairs per chunk: the caller's, else about an eighth of B*H.
+long long host_chunk(long long BH, int chunk_bh) {
+    long long cb = chunk_bh > 0 ? chunk_bh : (BH + 7) / 8;
+    return cb < BH ? cb : BH;
+}
+
+// Sizes accepted by the host-staged call; the slot arithmetic stays far
+// from size_t overflow.
+bool host_sizes_ok(int B, int H, int Nq, int Nk, int d, int n_modes, int chunk_bh) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || n_modes < 1 || n_modes > kHostMaxModes) return false;
+    if (d != 64 && d != 128) return false;
+    const long long BH = (long long)B * H;
+    if (BH > 0x7fffffffLL) return false;
+    const double cb = (double)host_chunk(BH, chunk_bh);
+    const double slot = cb * (3.0 * Nq + 2.0 * Nk) * d * 2.0 * (n_modes + 2) + 1e6;
+    return slot * kHostSlots < 1e18;
+}
+
+// Host (page-locked, pageable or managed) memory, i.e. not device memory.
+bool host_memory(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type != cudaMemoryTypeDevice;
+}
+
+bool device_memory(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+attn_status_t host_stage_state(HostStage** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    HostStage& h = g_host[dev];
+    if (!h.ready) {
+        if (cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h.entry, cudaEventDisableTiming) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        for (int s = 0; s < kHostSlots; ++s)
+            if (cudaEventCreateWithFlags(&h.in_done[s], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h.comp_done[s], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&h.out_done[s], cudaEventDisableTiming) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+        h.ready = true;
+    }
+    *out = &h;
+    return ATTN_OK;
 }
 
 }  // namespace
@@ -444,6 +542,102 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     p.c_scale = scale * 1.4426950408889634f;
     p.scale = scale;
     return from_cuda(launch_bwd(d, p, static_cast<cudaStream_t>(stream)));
+}
+
+size_t attn_fwd_host_workspace_size(int B, int H, int Nq, int Nk, int d, int n_modes, int chunk_bh) {
+    if (!host_sizes_ok(B, H, Nq, Nk, d, n_modes, chunk_bh)) return 0;
+    const long long cb = host_chunk((long long)B * H, chunk_bh);
+    return (size_t)kHostSlots * slot_layout(cb, Nq, Nk, d, n_modes).slot;
+}
+
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, int n_modes, const int* causal,
+                            void* const* o, float* const* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                            int chunk_bh, void* workspace, size_t workspace_bytes, void* stream) {
+    // ---- validation: nothing is enqueued on a bad argument
+    if (!q || !k || !v || !causal || !o) return ATTN_ERR_INVALID_ARG;
+    if (n_modes < 1 || n_modes > kHostMaxModes) return ATTN_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || (long long)B * H > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+    for (int m = 0; m < n_modes; ++m)
+        if (!o[m] || (causal[m] != 0 && causal[m] != 1)) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!host_sizes_ok(B, H, Nq, Nk, d, n_modes, chunk_bh)) return ATTN_ERR_INVALID_ARG;
+    const size_t need = attn_fwd_host_workspace_size(B, H, Nq, Nk, d, n_modes, chunk_bh);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    if (!host_memory(q) || !host_memory(k) || !host_memory(v)) return ATTN_ERR_INVALID_ARG;
+    for (int m = 0; m < n_modes; ++m)
+        if (!host_memory(o[m]) || (lse && lse[m] && !host_memory(lse[m]))) return ATTN_ERR_INVALID_ARG;
+    if (!device_memory(workspace)) return ATTN_ERR_WORKSPACE;
+
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    HostStage* hs = nullptr;
+    st = host_stage_state(&hs);
+    if (st != ATTN_OK) return st;
+
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const long long BH = (long long)B * H;
+    const long long cb = host_chunk(BH, chunk_bh);
+    const long long n_chunks = (BH + cb - 1) / cb;
+    const SlotLayout L = slot_layout(cb, Nq, Nk, d, n_modes);
+    const size_t q_bh = (size_t)Nq * d * 2, kv_bh = (size_t)Nk * d * 2, l_bh = (size_t)Nq * 4;
+    const uint8_t* hq = static_cast<const uint8_t*>(q);
+    const uint8_t* hk = static_cast<const uint8_t*>(k);
+    const uint8_t* hv = static_cast<const uint8_t*>(v);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+#define ATTN_CK(x)                                  \
+    do {                                            \
+        if ((x) != cudaSuccess) return ATTN_ERR_CUDA; \
+    } while (0)
+
+    // both copy streams start after the work already on the caller's stream
+    ATTN_CK(cudaEventRecord(hs->entry, cs));
+    ATTN_CK(cudaStreamWaitEvent(hs->s_in, hs->entry, 0));
+    ATTN_CK(cudaStreamWaitEvent(hs->s_out, hs->entry, 0));
+    for (long long c = 0; c < n_chunks; ++c) {
+        const int slot = (int)(c % kHostSlots);
+        const long long bh0 = c * cb;
+        const long long n = (BH - bh0) < cb ? (BH - bh0) : cb;
+        uint8_t* dq = ws + (size_t)slot * L.slot;
+        uint8_t* dk = dq + L.q;
+        uint8_t* dv = dk + L.kv;
+        uint8_t* dout0 = dv + L.kv;
+        // copy in
+        if (c >= kHostSlots) ATTN_CK(cudaStreamWaitEvent(hs->s_in, hs->comp_done[slot], 0));
+        ATTN_CK(cudaMemcpyAsync(dq, hq + bh0 * q_bh, n * q_bh, cudaMemcpyHostToDevice, hs->s_in));
+        ATTN_CK(cudaMemcpyAsync(dk, hk + bh0 * kv_bh, n * kv_bh, cudaMemcpyHostToDevice, hs->s_in));
+        ATTN_CK(cudaMemcpyAsync(dv, hv + bh0 * kv_bh, n * kv_bh, cudaMemcpyHostToDevice, hs->s_in));
+        ATTN_CK(cudaEventRecord(hs->in_done[slot], hs->s_in));
+        // compute: the chunk's n pairs as one [1, n] batch, one launch per mode
+        ATTN_CK(cudaStreamWaitEvent(cs, hs->in_done[slot], 0));
+        if (c >= kHostSlots) ATTN_CK(cudaStreamWaitEvent(cs, hs->out_done[slot], 0));
+        for (int m = 0; m < n_modes; ++m) {
+            uint8_t* dom = dout0 + (size_t)m * L.per_mode;
+            float* dlm = (lse && lse[m]) ? reinterpret_cast<float*>(dom + L.o) : nullptr;
+            st = prefill(dq, dk, dv, dom, dlm, 1, (int)n, Nq, Nk, d, scale, causal[m], false, 1.f, 1.f, 1.f, cs);
+            if (st != ATTN_OK) return st;
+        }
+        ATTN_CK(cudaEventRecord(hs->comp_done[slot], cs));
+        // copy out
+        ATTN_CK(cudaStreamWaitEvent(hs->s_out, hs->comp_done[slot], 0));
+        for (int m = 0; m < n_modes; ++m) {
+            uint8_t* dom = dout0 + (size_t)m * L.per_mode;
+            ATTN_CK(cudaMemcpyAsync(static_cast<uint8_t*>(o[m]) + bh0 * q_bh, dom, n * q_bh, cudaMemcpyDeviceToHost,
+                                    hs->s_out));
+            if (lse && lse[m])
+                ATTN_CK(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse[m]) + bh0 * l_bh, dom + L.o, n * l_bh,
+                                        cudaMemcpyDeviceToHost, hs->s_out));
+        }
+        ATTN_CK(cudaEventRecord(hs->out_done[slot], hs->s_out));
+    }
+    // later work on the caller's stream starts after the last copy out (the
+    // copy-out stream runs in order, so that covers every chunk)
+    ATTN_CK(cudaStreamWaitEvent(cs, hs->out_done[(n_chunks - 1) % kHostSlots], 0));
+#undef ATTN_CK
+    return ATTN_OK;
 }
 
 attn_status_t attn_device_status(void* stream) {

@@ -1,7 +1,7 @@
 /*
  * attn.h -- C ABI of the GB300 (sm_103a) exact-attention library.
  *
- * Three operations, all computing exact scaled-dot-product attention
+ * Every forward entry point computes exact scaled-dot-product attention
  *     O = softmax(scale * Q K^T) V
  * ("FlashAttention V3 实战: Hopper 架构下的 Paged KV Cache 协同优化",
  * section 一, the attention formula; "Capstone: CUDA Softmax 与 Attention
@@ -11,13 +11,16 @@
  * and probability matrices never reach device memory.
  *
  * Conventions shared by every entry point
- *   - All tensor pointers are DEVICE pointers owned by the caller.  The
- *     library allocates nothing and frees nothing; it keeps only per-device
- *     cached kernel attributes and one device status word (see
- *     attn_device_status).
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except
+ *     the tensors of attn_fwd_host, which live in host memory.  The
+ *     library allocates no memory and frees nothing; it keeps only
+ *     per-device cached kernel attributes, one device status word (see
+ *     attn_device_status) and, once attn_fwd_host has run on a device, that
+ *     call's two streams and ten events.
  *   - Layouts are dense row-major ("BHSD"): element (b, h, i, c) of a
  *     [B, H, N, d] tensor is at ((b*H + h)*N + i)*d + c.
- *   - Every pointer must be 16-byte aligned.
+ *   - Every device pointer must be 16-byte aligned (host pointers of
+ *     attn_fwd_host need no alignment).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls are asynchronous: they validate their arguments on the
  *     host, enqueue kernels and return; nothing synchronises.
@@ -243,6 +246,41 @@ size_t attn_bwd_workspace_size(int B, int H, int Nq, int d);
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                        const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
                        float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of device workspace attn_fwd_host needs (0 on invalid sizes): three
+ * chunk slots, each holding one chunk of Q, K, V and, per mask mode, one
+ * chunk of O and LSE.  chunk_bh <= 0 asks for the default chunk. */
+size_t attn_fwd_host_workspace_size(int B, int H, int Nq, int Nk, int d, int n_modes, int chunk_bh);
+
+/* Dense bf16 prefill with the inputs and outputs in HOST memory: the
+ * attn_fwd computation for each of n_modes mask modes over the same Q, K, V,
+ * with the host<->device copies inside the call.
+ *   q: host bf16 [B, H, Nq, d]; k, v: host bf16 [B, H, Nk, d]   (read only)
+ *   causal[i] in {0, 1} for i < n_modes, 1 <= n_modes <= 8;
+ *   o[i]: host bf16 [B, H, Nq, d]; lse[i]: host fp32 [B, H, Nq] or NULL.
+ *   chunk_bh: batch-head pairs per chunk (<= 0: about an eighth of B*H).
+ *   workspace: DEVICE memory of attn_fwd_host_workspace_size() bytes,
+ *   16-byte aligned.
+ * The (b, h) range is cut into chunks of chunk_bh pairs.  Each chunk is
+ * copied in on one internal stream, computed on `stream` (one attn_fwd
+ * kernel per mode), and copied out on a second internal stream, so the two
+ * copy directions and the kernels of neighbouring chunks overlap.  Each
+ * (b, h) problem is computed by the same kernel as attn_fwd, so the outputs
+ * are bit-identical to attn_fwd on device copies of the inputs.  The copies
+ * overlap only when the host buffers are page-locked (cudaHostAlloc or
+ * cudaHostRegister); pageable buffers give the same results serially.
+ * Ordering: the copies start after the work already enqueued on `stream`;
+ * work enqueued on `stream` after the call starts after every output has
+ * landed in host memory.  Synchronise `stream` before reading the outputs.
+ * Resources: the first call on a device creates two streams and ten events
+ * there, kept for the life of the process.  Calls on one device are
+ * serialised by a host lock while they enqueue.
+ * Errors: ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED / ATTN_ERR_WORKSPACE
+ * before anything is enqueued (also when a pointer is device memory);
+ * ATTN_ERR_CUDA if a copy or launch fails part-way (outputs undefined). */
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, int n_modes, const int* causal,
+                            void* const* o, float* const* lse, int B, int H, int Nq, int Nk, int d, float scale,
+                            int chunk_bh, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, then reads and clears the calling device's status
  * word.  Kernels set it when a bounded internal wait gives up

@@ -30,6 +30,7 @@ def test_header_declares_the_entry_points():
                                   "attn_paged_fwd", "attn_paged_fwd_workspace_size",
                                   "attn_varlen_fwd", "attn_varlen_fwd_workspace_size",
                                   "attn_bwd", "attn_bwd_workspace_size",
+                                  "attn_fwd_host", "attn_fwd_host_workspace_size",
                                   "attn_device_status", "attn_status_string"])
 
 
@@ -178,3 +179,37 @@ def test_bwd_validation(L):
     assert attn.attn_bwd(**dict(base, d=96)) == attn.ATTN_ERR_UNSUPPORTED
     assert attn.attn_bwd(**dict(base, workspace_bytes=ws - 4)) == attn.ATTN_ERR_WORKSPACE
     assert attn.attn_bwd(**dict(base, causal=3)) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_fwd_host_workspace_and_validation(L):
+    """Slot sizes of the host-staged prefill (three slots, each rounded to 256-byte buffers) and the
+    checks it makes before touching any device or host memory."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    cb = 3
+    slot = r256(cb * 300 * 128 * 2) + 2 * r256(cb * 200 * 128 * 2) + 2 * (r256(cb * 300 * 128 * 2) + r256(cb * 300 * 4))
+    ws = attn.attn_fwd_host_workspace_size(2, 4, 300, 200, 128, 2, cb)
+    assert ws == 3 * slot
+    # default chunk: about an eighth of B*H (here one pair); a chunk larger than B*H is clipped to it
+    assert attn.attn_fwd_host_workspace_size(2, 4, 300, 200, 128, 1, 0) == \
+        attn.attn_fwd_host_workspace_size(2, 4, 300, 200, 128, 1, 1)
+    assert attn.attn_fwd_host_workspace_size(2, 4, 300, 200, 128, 1, 100) == \
+        attn.attn_fwd_host_workspace_size(2, 4, 300, 200, 128, 1, 8)
+    for bad in [(2, 4, 300, 200, 96, 1, 1), (2, 4, 300, 200, 128, 0, 1), (2, 4, 300, 200, 128, 9, 1),
+                (0, 4, 300, 200, 128, 1, 1), (2, 4, 0, 200, 128, 1, 1)]:
+        assert attn.attn_fwd_host_workspace_size(*bad) == 0
+    modes = (ctypes.c_int * 2)(0, 1)
+    outs = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    base = dict(q=FAKE, k=FAKE, v=FAKE, n_modes=2, causal=ctypes.addressof(modes), o=ctypes.addressof(outs),
+                lse=None, B=2, H=4, Nq=300, Nk=200, d=128, scale=0.088, chunk_bh=cb, workspace=FAKE,
+                workspace_bytes=ws, stream=None)
+    assert attn.attn_fwd_host(**dict(base, v=None)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_host(**dict(base, n_modes=0)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_host(**dict(base, scale=-1.0)) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_fwd_host(**dict(base, d=96)) == attn.ATTN_ERR_UNSUPPORTED
+    assert attn.attn_fwd_host(**dict(base, workspace_bytes=ws - 1)) == attn.ATTN_ERR_WORKSPACE
+    assert attn.attn_fwd_host(**dict(base, workspace=FAKE + 4)) == attn.ATTN_ERR_WORKSPACE
+    bad_modes = (ctypes.c_int * 2)(0, 2)
+    assert attn.attn_fwd_host(**dict(base, causal=ctypes.addressof(bad_modes))) == attn.ATTN_ERR_INVALID_ARG
+    no_out = (ctypes.c_void_p * 2)(FAKE, None)
+    assert attn.attn_fwd_host(**dict(base, o=ctypes.addressof(no_out))) == attn.ATTN_ERR_INVALID_ARG
