@@ -434,7 +434,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int j = blockIdx.x, bh = blockIdx.y;
+    // CTAs are dispatched in linear block order.  Non-causal: the key blocks
+    // of one head are adjacent, so concurrent CTAs share that head's Q and dO
+    // in L2.  Causal: heaviest first (key block j sees the query blocks from
+    // first_qblock(j) on, fewer as j grows), so the short CTAs fill the tail.
+    int j = blockIdx.x, bh = blockIdx.y;
+    if (p.causal) {
+        const long long lin = (long long)blockIdx.y * gridDim.x + blockIdx.x;
+        j = (int)(lin / p.BH);
+        bh = (int)(lin % p.BH);
+    }
     const int i0 = first_qblock(p, j);
     const int nqb = p.n_qblocks - i0 > 0 ? p.n_qblocks - i0 : 0;
 
