@@ -156,6 +156,80 @@ bool make_paged_map(CUtensorMap* map, const void* base, int d, long long heads, 
     return r == CUDA_SUCCESS;
 }
 
+// ---- ragged prefill: the prefill kernel over variable-length sequences.
+//
+// Launches whose sequences bring at least kRaggedMinQ query tokens run on
+// the prefill kernel in its ragged mode (two 128-row tiles of one query
+// head per unit, the keys of its KV head streamed once for both); shorter
+// ones -- decode steps, short chunks -- on the paged kernel, which packs the
+// G query heads of a KV head into one tile.
+constexpr int kRaggedMinQ = 128;
+
+bool use_ragged(int max_q_len) { return max_q_len >= kRaggedMinQ; }
+
+// O map of the ragged mode over token-major [total_q, H, d]: dims (d, H,
+// total_q), box (32 elements, 1 head, 32 tokens), no swizzle.
+bool make_ragged_out_map(CUtensorMap* map, void* base, int d, long long heads, long long tokens) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    cuuint32_t box[3] = {32u, 1u, 32u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Keys: paged (block_table non-null: rows = num_pages * page_size slots,
+// R = min(page_size, 128) rows per box) or contiguous (rows = total_k, R = 128).
+attn_status_t ragged_prefill(DeviceState* ds, const void* q, const void* k, const void* v,
+                             const int32_t* block_table, const int32_t* cu_q, const int32_t* seq_lens,
+                             const int32_t* cu_k, int B, int total_q, int max_q_len, int H, int H_kv, int d,
+                             int page_size, int max_pages, int num_pages, long long kv_rows, int kv_cap, float scale,
+                             int causal, void* o, float* lse, void* workspace, cudaStream_t stream) {
+    PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    const int R = block_table ? (page_size < 128 ? page_size : 128) : 128;
+    if (!make_paged_map(&p.tm_q, q, d, H, total_q, 1, 128) || !make_paged_map(&p.tm_k, k, d, H_kv, kv_rows, 1, R) ||
+        !make_paged_map(&p.tm_v, v, d, H_kv, kv_rows, 1, R) || !make_ragged_out_map(&p.tm_o, o, d, H, total_q))
+        return ATTN_ERR_CUDA;
+    int* n_listed = static_cast<int*>(workspace);
+    int4* units = reinterpret_cast<int4*>(static_cast<char*>(workspace) + 256);
+    p.lse = lse;
+    p.status = ds->status;
+    p.causal = causal;
+    p.c_scale = scale * 1.4426950408889634f;
+    p.o_scale = 1.f;
+    p.units = units;
+    p.n_listed = n_listed;
+    p.block_table = block_table;
+    p.o = static_cast<uint16_t*>(o);
+    p.H = H;
+    p.G = H / H_kv;
+    p.page_size = page_size;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.rows_per_box = R;
+    p.kv_rows = (int)kv_rows;
+    RaggedSched sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.cu_q = cu_q;
+    sp.seq_lens = block_table ? seq_lens : nullptr;
+    sp.cu_k = block_table ? nullptr : cu_k;
+    sp.units = units;
+    sp.n_listed = n_listed;
+    sp.status = ds->status;
+    sp.B = B;
+    sp.H = H;
+    sp.total_q = total_q;
+    sp.max_q_len = max_q_len;
+    sp.kv_cap = kv_cap;
+    sp.causal = causal;
+    const long long upper = (long long)B * ((max_q_len + 255) / 256) * H;  // units the list can hold
+    const int grid = upper < ds->sm_count ? (int)upper : ds->sm_count;     // persistent: one CTA per SM
+    return from_cuda(launch_ragged_prefill(d, sp, p, grid, stream));
+}
+
 // ---- host-staged prefill: copy in, compute, copy out, chunk by chunk.
 //
 // The (b, h) range is cut into chunks.  Chunk c uses workspace slot
@@ -338,6 +412,7 @@ attn_status_t attn_paged_decode(const void* q, const void* k_cache, const void* 
 size_t attn_paged_fwd_workspace_size(int B, int total_q, int max_q_len, int H, int H_kv, int d, int page_size,
                                      int max_pages_per_seq) {
     if (paged_sizes_ok(B, total_q, max_q_len, H, H_kv, d, page_size, max_pages_per_seq) != ATTN_OK) return 0;
+    if (use_ragged(max_q_len)) return ragged_workspace_bytes(B, max_q_len, H);
     return paged_plan(total_q, max_q_len, B, H, H_kv, d, page_size, max_pages_per_seq).workspace_bytes;
 }
 
@@ -357,6 +432,18 @@ attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_c
     auto a4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
     if (!a4(block_table) || !a4(seq_lens) || (cu_seqlens_q && !a4(cu_seqlens_q)) || (lse && !a4(lse)))
         return ATTN_ERR_INVALID_ARG;
+    if (use_ragged(max_q_len)) {
+        const size_t need = ragged_workspace_bytes(B, max_q_len, H);
+        if ((long long)B * ((max_q_len + 255) / 256) * H > 0x3fffffffLL) return ATTN_ERR_INVALID_ARG;
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+        DeviceState* ds = nullptr;
+        st = device_state(&ds);
+        if (st != ATTN_OK) return st;
+        return ragged_prefill(ds, q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, nullptr, B, total_q,
+                              max_q_len, H, H_kv, d, page_size, max_pages_per_seq, num_pages,
+                              (long long)num_pages * page_size, max_pages_per_seq * page_size, scale, causal, o, lse,
+                              workspace, static_cast<cudaStream_t>(stream));
+    }
     const PagedPlan pl = paged_plan(total_q, max_q_len, B, H, H_kv, d, page_size, max_pages_per_seq);
     if (pl.n_units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < pl.workspace_bytes || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
@@ -413,6 +500,7 @@ size_t attn_varlen_fwd_workspace_size(int B, int total_q, int max_q_len, int max
     if (max_k_len < 1) return 0;
     const int max_blocks = (int)(((long long)max_k_len + 127) / 128);
     if (paged_sizes_ok(B, total_q, max_q_len, H, H_kv, d, 128, max_blocks) != ATTN_OK) return 0;
+    if (use_ragged(max_q_len)) return ragged_workspace_bytes(B, max_q_len, H);
     return paged_plan(total_q, max_q_len, B, H, H_kv, d, 128, max_blocks).workspace_bytes;
 }
 
@@ -431,6 +519,17 @@ attn_status_t attn_varlen_fwd(const void* q, const void* k, const void* v, const
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
     auto a4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
     if (!a4(cu_seqlens_q) || !a4(cu_seqlens_k) || (lse && !a4(lse))) return ATTN_ERR_INVALID_ARG;
+    if (use_ragged(max_q_len)) {
+        const size_t need = ragged_workspace_bytes(B, max_q_len, H);
+        if ((long long)B * ((max_q_len + 255) / 256) * H > 0x3fffffffLL) return ATTN_ERR_INVALID_ARG;
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+        DeviceState* ds = nullptr;
+        st = device_state(&ds);
+        if (st != ATTN_OK) return st;
+        return ragged_prefill(ds, q, k, v, nullptr, cu_seqlens_q, nullptr, cu_seqlens_k, B, total_q, max_q_len, H,
+                              H_kv, d, 128, max_blocks, 0, total_k, total_k, scale, causal, o, lse, workspace,
+                              static_cast<cudaStream_t>(stream));
+    }
     const PagedPlan pl = paged_plan(total_q, max_q_len, B, H, H_kv, d, 128, max_blocks);
     if (pl.n_units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < pl.workspace_bytes || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;

@@ -23,6 +23,15 @@ struct PrefillParams {
     int n_units;        // n_pairs * B * H
     float c_scale;      // scale * log2(e) [* q_descale * k_descale]
     float o_scale;      // 1 [or v_descale]
+    // ---- ragged mode only (variable-length sequences, keys contiguous or paged)
+    const int4* units;       // 2 int4 per listed unit: (s, pair, h, q_start), (q_len, kv_len, kv_start, 0)
+    const int* n_listed;     // number of listed units (written by the schedule pass)
+    const int32_t* block_table;  // [B, max_pages] page ids; nullptr: contiguous keys from row kv_start
+    uint16_t* o;             // bf16 [total_q, H, d] (rows of a tile that straddles a sequence end)
+    int H, G;                // query heads, query heads per KV head
+    int page_size, max_pages, num_pages;
+    int rows_per_box;        // key rows per TMA box: min(page_size, 128), or 128 for contiguous keys
+    int kv_rows;             // rows of the key tensor: the first row past it reads as zeros
 };
 
 constexpr int kPrefillThreads = 352;  // 2 MMA issuer warps + TMA warp + 2 softmax warpgroups
@@ -30,6 +39,24 @@ constexpr int kPrefillThreads = 352;  // 2 MMA issuer warps + TMA warp + 2 softm
 int prefill_smem_bytes(int d, bool fp8);
 // grid = number of persistent CTAs (at most one per SM and at most n_units)
 cudaError_t launch_prefill(int d, bool fp8, const PrefillParams& p, int grid, cudaStream_t stream);
+
+// Ragged prefill: the prefill kernel over variable-length sequences of
+// token-major tensors (q, o [total_q, H, d]; keys [rows, H_kv, d], contiguous
+// per sequence or gathered through a block table).  A one-CTA schedule pass
+// lists the units (sequence, query-tile pair, head), longest first.
+struct RaggedSched {
+    const int32_t* cu_q;      // [B + 1] query offsets
+    const int32_t* seq_lens;  // [B] key counts (paged keys), or nullptr
+    const int32_t* cu_k;      // [B + 1] key offsets (contiguous keys), or nullptr
+    int4* units;              // out: 2 int4 per unit
+    int* n_listed;            // out
+    unsigned* status;
+    int B, H, total_q, max_q_len, kv_cap, causal;  // kv_cap: largest valid key count (paged) or key rows
+};
+// bytes of workspace the ragged path needs for these sizes (unit list + count)
+size_t ragged_workspace_bytes(int B, int max_q_len, int H);
+cudaError_t launch_ragged_prefill(int d, const RaggedSched& sp, const PrefillParams& p, int grid,
+                                  cudaStream_t stream);
 
 // Paged decode: split kernel writes per-split partials, merge kernel combines.
 struct DecodeParams {

@@ -39,6 +39,8 @@
 // when the new block max exceeds it by more than kTau; O and l share that
 // stale max so O / l is unchanged (the merge identity of section 2.2 step 4
 // holds for any common reference point), and p stays <= 2^kTau.
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "tile_mma.cuh"
@@ -97,6 +99,14 @@ struct Unit {
     int q0[2], rows[2], n[2];
 };
 
+// Ragged mode: also the unit's sequence, head and extents.
+struct RaggedUnit : Unit {
+    int s, h, q_start, kv_start, Nq, Nk;
+};
+
+template <bool RAGGED>
+using UnitOf = typename std::conditional<RAGGED, RaggedUnit, Unit>::type;
+
 // Number of KV blocks query tile [q0, q0 + rows) needs (0 = nothing visible).
 __device__ __forceinline__ int tile_blocks(int q0, int rows, int Nq, int Nk, int causal) {
     if (rows <= 0) return 0;
@@ -126,20 +136,51 @@ __device__ __forceinline__ Unit unit_geometry(const PrefillParams& p, int u) {
         g.n[t] = tile_blocks(g.q0[t], g.rows[t], p.Nq, p.Nk, p.causal);
     }
     g.J = g.n[0] > g.n[1] ? g.n[0] : g.n[1];
+    return g;  // the ragged-mode fields stay unset: the dense mode reads the launch's extents
+}
+
+// Ragged mode: unit u of the list the schedule pass wrote, entries
+// (s, pair, h, q_start) and (q_len, kv_len, kv_start, 0).
+__device__ __forceinline__ RaggedUnit ragged_unit(const PrefillParams& p, int u) {
+    const int4 a = __ldg(p.units + 2 * u), c = __ldg(p.units + 2 * u + 1);
+    RaggedUnit g;
+    g.s = a.x;
+    g.h = a.z;
+    g.bh = a.z;
+    g.q_start = a.w;
+    g.Nq = c.x;
+    g.Nk = c.y;
+    g.kv_start = c.z;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        g.q0[t] = (2 * a.y + t) * 128;
+        const int rr = g.Nq - g.q0[t];
+        g.rows[t] = rr < 0 ? 0 : (rr > 128 ? 128 : rr);
+        g.n[t] = tile_blocks(g.q0[t], g.rows[t], g.Nq, g.Nk, p.causal);
+    }
+    g.J = g.n[0] > g.n[1] ? g.n[0] : g.n[1];
     return g;
+}
+
+template <bool RAGGED>
+__device__ __forceinline__ UnitOf<RAGGED> unit_at(const PrefillParams& p, int u) {
+    if constexpr (RAGGED)
+        return ragged_unit(p, u);
+    else
+        return unit_geometry(p, u);
 }
 
 // The r-th unit of this CTA in snake order (rounds of gridDim.x units, every
 // other round reversed), or -1 when the CTA has no more units.  `round_` is
 // advanced past rounds in which this CTA gets nothing.
-__device__ __forceinline__ int next_unit(const PrefillParams& p, int& round_) {
+__device__ __forceinline__ int next_unit(int n_units, int& round_) {
     const int G = (int)gridDim.x, c = (int)blockIdx.x;
     for (;;) {
         const long long base = (long long)round_ * G;
-        if (base >= p.n_units) return -1;
+        if (base >= n_units) return -1;
         const int u = (int)base + ((round_ & 1) ? (G - 1 - c) : c);
         ++round_;
-        if (u < p.n_units) return u;
+        if (u < n_units) return u;
     }
 }
 
@@ -169,8 +210,9 @@ __device__ __forceinline__ bool load_kv(const PrefillParams& p, uint8_t* smem, c
     return true;
 }
 
-template <int D, bool FP8>
-__device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars& b, volatile int* abort_flag) {
+template <int D, bool FP8, bool RAGGED>
+__device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars& b, volatile int* abort_flag,
+                              int n_units) {
     using C = Cfg<D, FP8>;
     tma_prefetch_map(&p.tm_q);
     tma_prefetch_map(&p.tm_k);
@@ -179,8 +221,8 @@ __device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars&
     int qcnt[2] = {0, 0};
     int round_ = 0;
     bool ok = true;
-    for (int u = next_unit(p, round_); ok && u >= 0; u = next_unit(p, round_)) {
-        const Unit g = unit_geometry(p, u);
+    for (int u = next_unit(RAGGED ? n_units : p.n_units, round_); ok && u >= 0; u = next_unit(RAGGED ? n_units : p.n_units, round_)) {
+        const UnitOf<RAGGED> g = unit_at<RAGGED>(p, u);
         for (int j = 0; ok && j < g.J; ++j) {
             ok = load_kv<D, FP8>(p, smem, b, abort_flag, kv_idx, j, g.bh, false) &&
                  load_kv<D, FP8>(p, smem, b, abort_flag, kv_idx, j, g.bh, true);
@@ -211,6 +253,107 @@ __device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars&
         drain_wait(&b.kv_full[idx % C::NST], (uint32_t)((idx / C::NST) & 1), p.status);
 }
 
+// Ragged mode producer (whole warp): the same stream as producer_role -- K_j,
+// V_j of every KV block, the unit's Q tiles after its first block -- with
+// each 128-key block gathered from 128 / R boxes of R rows: through the block
+// table (paged keys; the lanes look up 32 page ids at a time) or from the
+// sequence's contiguous rows.  A box past the sequence's keys, or naming an
+// out-of-range page, reads the zero fill past the end of the key tensor.
+template <int D>
+__device__ void ragged_producer_role(const PrefillParams& p, uint8_t* smem, const Bars& b, volatile int* abort_flag,
+                                     int lane, int n_units) {
+    using C = Cfg<D, false>;
+    if (lane == 0) {
+        tma_prefetch_map(&p.tm_q);
+        tma_prefetch_map(&p.tm_k);
+        tma_prefetch_map(&p.tm_v);
+    }
+    const int R = p.rows_per_box;
+    const int LPB = 128 / R;  // boxes per block (1..16)
+    const int oob = p.kv_rows;
+    int kv_idx = 0;
+    int qcnt[2] = {0, 0};
+    int round_ = 0;
+    bool ok = true;
+    for (int u = next_unit(n_units, round_); ok && u >= 0; u = next_unit(n_units, round_)) {
+        const RaggedUnit g = ragged_unit(p, u);
+        const int kvh = g.h / p.G;
+        int my_row = oob;
+        for (int j = 0; ok && j < g.J; ++j) {
+            const int box0 = j * LPB;
+            if ((box0 & 31) == 0) {  // lane i: the cache row of box box0 + i
+                const int bi = box0 + lane;
+                const long long key = (long long)bi * R;
+                int row = oob;
+                if (bi < g.J * LPB && key < g.Nk) {
+                    if (p.block_table != nullptr) {
+                        const int pg = (int)(key / p.page_size);
+                        const int id = __ldg(p.block_table + (size_t)g.s * p.max_pages + pg);
+                        if (id >= 0 && id < p.num_pages)
+                            row = id * p.page_size + (int)(key % p.page_size);
+                        else
+                            atomicOr(p.status, 1u << kStatusDeviceData);
+                    } else {
+                        row = g.kv_start + (int)key;
+                    }
+                }
+                my_row = row;
+            }
+            int rows[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) rows[i] = __shfl_sync(0xffffffffu, my_row, (box0 + (i < LPB ? i : 0)) & 31);
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                if (lane == 0) {
+                    const int slot = kv_idx % C::NST, round = kv_idx / C::NST;
+                    if (round > 0) ok = wait_bar(&b.kv_empty[slot], (uint32_t)((round - 1) & 1), abort_flag, p.status);
+                    if (ok) {
+                        bar_arrive_expect_tx(&b.kv_full[slot], C::TILE_BYTES);
+                        const CUtensorMap* map = kv ? &p.tm_v : &p.tm_k;
+                        uint8_t* dst = smem + C::OFF_KV + slot * C::TILE_BYTES;
+                        for (int i = 0; i < LPB; ++i)
+#pragma unroll
+                            for (int pn = 0; pn < C::NPANEL; ++pn)
+                                tma_load_3d(dst + pn * C::PANEL_BYTES + i * R * 128, map, &b.kv_full[slot],
+                                            pn * C::PANEL, kvh, rows[i]);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                ++kv_idx;
+            }
+            if (!ok || j != 0) continue;
+            // the unit's first K/V block is in flight; now its query tiles
+            if (lane == 0) {
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (g.n[t] == 0) continue;
+                    if (qcnt[t] > 0 &&
+                        !wait_bar(&b.q_empty[t], (uint32_t)((qcnt[t] - 1) & 1), abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    bar_arrive_expect_tx(&b.q_full[t], C::TILE_BYTES);
+#pragma unroll
+                    for (int pn = 0; pn < C::NPANEL; ++pn)
+                        tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q, &b.q_full[t],
+                                    pn * C::PANEL, g.h, g.q_start + g.q0[t]);
+                    ++qcnt[t];
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+    }
+    // Drain: every copy this warp started must land before the CTA exits.
+    if (lane == 0) {
+        for (int t = 0; t < 2; ++t)
+            if (qcnt[t] > 0) drain_wait(&b.q_full[t], (uint32_t)((qcnt[t] - 1) & 1), p.status);
+        for (int idx = kv_idx - C::NST > 0 ? kv_idx - C::NST : 0; idx < kv_idx; ++idx)
+            drain_wait(&b.kv_full[idx % C::NST], (uint32_t)((idx / C::NST) & 1), p.status);
+    }
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------- MMA issuers
 
 // MMA issuers: warp t issues query tile t's GEMMs.  The two issuers take
@@ -223,9 +366,9 @@ __device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars&
 // the pipe busy; the waits of an issuing thread otherwise leave the pipe idle.
 // Slots of the K/V ring are released by both issuers (two arrivals); a tile
 // that needs no more blocks of the unit releases with a plain arrive.
-template <int D, bool FP8>
+template <int D, bool FP8, bool RAGGED>
 __device__ void mma_role(const PrefillParams& p, uint8_t* smem, const Bars& b, volatile int* abort_flag,
-                         uint32_t tmem, int t) {
+                         uint32_t tmem, int t, int n_units) {
     using C = Cfg<D, FP8>;
     const uint32_t sbase = smem_u32(smem);
     const uint64_t q_desc = sdesc_sw128(sbase + C::OFF_Q + (uint32_t)(t * C::TILE_BYTES), 16, 1024);
@@ -255,8 +398,8 @@ __device__ void mma_role(const PrefillParams& p, uint8_t* smem, const Bars& b, v
     // while the other issuer's GEMMs occupy the pipe.
     auto pass_turn = [&]() { bar_arrive(&b.turn[t ^ 1]); };
     int round_ = 0;
-    for (int u = next_unit(p, round_); u >= 0; u = next_unit(p, round_)) {
-        const Unit g = unit_geometry(p, u);
+    for (int u = next_unit(RAGGED ? n_units : p.n_units, round_); u >= 0; u = next_unit(RAGGED ? n_units : p.n_units, round_)) {
+        const UnitOf<RAGGED> g = unit_at<RAGGED>(p, u);
         const int nt = g.n[t], J = g.J;
         if (J == 0) continue;
         // ---- start group: S_t(0)
@@ -325,26 +468,36 @@ __device__ void mma_role(const PrefillParams& p, uint8_t* smem, const Bars& b, v
 
 // ---------------------------------------------------------------- softmax + epilogue
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool RAGGED>
 __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& b, volatile int* abort_flag,
-                             uint32_t tmem, int t, int wq, int lane) {
+                             uint32_t tmem, int t, int wq, int lane, int n_units) {
     using C = Cfg<D, FP8>;
     const int r = wq * 32 + lane;  // row within the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::tm_s(t);
     const uint32_t tO = tmem + lane_off + C::tm_o(t);
-    const int off = p.Nk - p.Nq;
     const float cs = p.c_scale;
     uint8_t* ost = smem + C::OFF_OST + (t * 4 + wq) * C::OST_WARP_BYTES;
     const uint32_t ost_u = smem_u32(ost);
     uint32_t sblk = 0, units = 0, nstore = 0;
-    int round_ = 0;
+    int round_ = 0, kv_base = 0;
     bool ok = true;
 
-    for (int u = next_unit(p, round_); ok && u >= 0; u = next_unit(p, round_)) {
-        const Unit g = unit_geometry(p, u);
+    for (int u = next_unit(RAGGED ? n_units : p.n_units, round_); ok && u >= 0; u = next_unit(RAGGED ? n_units : p.n_units, round_)) {
+        const UnitOf<RAGGED> g = unit_at<RAGGED>(p, u);
         const int q0 = g.q0[t], rows = g.rows[t], nt = g.n[t], bh = g.bh;
+        const int kvb = kv_base;  // the unit's first K/V stream index
+        kv_base += 2 * g.J;
         if (rows <= 0) continue;  // tile lies entirely past Nq
+        int Nq_u, Nk_u;  // the unit's sequence
+        if constexpr (RAGGED) {
+            Nq_u = g.Nq;
+            Nk_u = g.Nk;
+        } else {
+            Nq_u = p.Nq;
+            Nk_u = p.Nk;
+        }
+        const int off = Nk_u - Nq_u;
         const int row = q0 + r;
         const long long limit = (long long)row + off;  // last visible key (causal)
         float m = -INFINITY, l = 0.f;
@@ -364,11 +517,11 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
 
             const int kbase = it * 128;
             const bool need_mask =
-                (kbase + 128 > p.Nk) || (p.causal && (long long)kbase + 127 > (long long)q0 + off);
+                (kbase + 128 > Nk_u) || (p.causal && (long long)kbase + 127 > (long long)q0 + off);
             if (need_mask) {
                 // visible columns of this row: [0, bound), the keys up to
                 // min(Nk - 1, limit) (causal) or Nk - 1
-                long long last = (long long)p.Nk - 1;
+                long long last = (long long)Nk_u - 1;
                 if (p.causal && limit < last) last = limit;
                 long long bl = last - kbase + 1;
                 const int bound = bl < 0 ? 0 : (bl > 128 ? 128 : (int)bl);
@@ -458,6 +611,28 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
                     tmem_st32(tO + 32 * ch, o);
                 }
             }
+            if constexpr (RAGGED) {
+                // Keys past the sequence in this block: clear their V rows (a
+                // partial last page holds arbitrary bytes, maybe NaN, and
+                // 0 * NaN would poison P V).  The tile whose PV reads the
+                // block first clears it: tile 0 while it is active, else tile 1.
+                if (kbase + 128 > g.Nk && (t == 0 || it >= g.n[0])) {
+                    const int iV = kvb + 2 * it + 1;
+                    ok = __all_sync(0xffffffffu, wait_bar(&b.kv_full[iV % C::NST], (uint32_t)((iV / C::NST) & 1),
+                                                          abort_flag, p.status));
+                    if (!ok) break;
+                    if (kbase + r >= g.Nk) {
+                        const uint32_t vrow =
+                            smem_u32(smem + C::OFF_KV + (iV % C::NST) * C::TILE_BYTES) + (uint32_t)(r * 128);
+#pragma unroll
+                        for (int pn = 0; pn < C::NPANEL; ++pn)
+#pragma unroll
+                            for (int cb = 0; cb < 128; cb += 16)
+                                st_shared_v4(vrow + (uint32_t)(pn * C::PANEL_BYTES + cb), 0u, 0u, 0u, 0u);
+                    }
+                    fence_async_smem();
+                }
+            }
             tmem_st_wait();
             tc_fence_before();
             bar_arrive(&b.p_full[t]);
@@ -483,7 +658,8 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
         }
         const float m_use = (m == -INFINITY) ? 0.f : m;
         const float inv = (l > 0.f) ? p.o_scale / l : 0.f;
-        const bool warp_rows = q0 + wq * 32 < p.Nq;  // some row of this warp is inside the tensor
+        const bool warp_rows = q0 + wq * 32 < Nq_u;        // some row of this warp is inside the sequence
+        const bool warp_full = !RAGGED || q0 + wq * 32 + 32 <= Nq_u;  // ragged: all 32 (else direct stores)
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
             const uint32_t buf = ost_u + (nstore & 1u) * 2048u;
@@ -494,26 +670,55 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
             for (int i = 0; i < 16; ++i)
                 w[i] = pack_bf16(__uint_as_float(o[32 * ch + 2 * i]) * inv,
                                  __uint_as_float(o[32 * ch + 2 * i + 1]) * inv);
+            if constexpr (!RAGGED) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                st_shared_v4(buf + (uint32_t)(lane * 64 + i * 16), w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                if (warp_rows) tma_store_3d(&p.tm_o, ost + (nstore & 1u) * 2048u, ch * 32, q0 + wq * 32, bh);
-                tma_store_commit();  // one (possibly empty) group per buffer use keeps the count exact
+                for (int i = 0; i < 4; ++i)
+                    st_shared_v4(buf + (uint32_t)(lane * 64 + i * 16), w[4 * i], w[4 * i + 1], w[4 * i + 2],
+                                 w[4 * i + 3]);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp_rows) tma_store_3d(&p.tm_o, ost + (nstore & 1u) * 2048u, ch * 32, q0 + wq * 32, bh);
+                    tma_store_commit();  // one (possibly empty) group per buffer use keeps the count exact
+                }
+            } else {
+                if (warp_full) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_shared_v4(buf + (uint32_t)(lane * 64 + i * 16), w[4 * i], w[4 * i + 1], w[4 * i + 2],
+                                     w[4 * i + 3]);
+                    fence_async_smem();
+                } else if (r < rows) {  // the warp straddles the sequence end: this row directly
+                    uint4* dst =
+                        reinterpret_cast<uint4*>(p.o + ((size_t)(g.q_start + row) * p.H + g.h) * D + ch * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    if (warp_rows && warp_full)
+                        tma_store_3d(&p.tm_o, ost + (nstore & 1u) * 2048u, ch * 32, g.h, g.q_start + q0 + wq * 32);
+                    tma_store_commit();  // one (possibly empty) group per buffer use keeps the count exact
+                }
             }
             ++nstore;
         }
-        if (p.lse != nullptr && r < rows)
-            p.lse[(size_t)bh * p.Nq + row] = (l > 0.f) ? (m_use + lg2(l)) * kLn2 : -INFINITY;
+        if (p.lse != nullptr && r < rows) {
+            size_t li;
+            if constexpr (RAGGED)
+                li = (size_t)(g.q_start + row) * p.H + g.h;
+            else
+                li = (size_t)bh * p.Nq + row;
+            p.lse[li] = (l > 0.f) ? (m_use + lg2(l)) * kLn2 : -INFINITY;
+        }
     }
     if (lane == 0) tma_store_wait_all();
 }
 
 // ---------------------------------------------------------------- kernel
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool RAGGED>
 __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p) {
     using C = Cfg<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
@@ -567,21 +772,27 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // ragged mode: the schedule pass (an earlier kernel of the stream) wrote the unit count
+    const int n_units = RAGGED ? __ldg(p.n_listed) : p.n_units;
 
     if (warp >= 3) {
         // warps 3-6: tile 0, warps 7-10: tile 1; a warp reaches TMEM lanes 32*(warp % 4)..+31
-        softmax_role<D, FP8>(p, smem, b, abort_flag, tmem, (warp - 3) >> 2, warp & 3, lane);
+        softmax_role<D, FP8, RAGGED>(p, smem, b, abort_flag, tmem, (warp - 3) >> 2, warp & 3, lane, n_units);
     } else if (warp < 2) {
         if (lane == 0) {
-            mma_role<D, FP8>(p, smem, b, abort_flag, tmem, warp);
+            mma_role<D, FP8, RAGGED>(p, smem, b, abort_flag, tmem, warp, n_units);
             // every issued MMA must finish before tensor memory is released
             tc_commit(&b.done[warp]);
             drain_wait(&b.done[warp], 0, p.status);
         }
         __syncwarp();
     } else {
-        if (lane == 0) producer_role<D, FP8>(p, smem, b, abort_flag);
-        __syncwarp();
+        if constexpr (RAGGED) {
+            ragged_producer_role<D>(p, smem, b, abort_flag, lane, n_units);
+        } else {
+            if (lane == 0) producer_role<D, FP8, RAGGED>(p, smem, b, abort_flag, n_units);
+            __syncwarp();
+        }
     }
 
     tc_fence_before();
@@ -592,14 +803,105 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_kernel(const __gri
     }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool RAGGED = false>
 cudaError_t launch_one(const PrefillParams& p, int grid, cudaStream_t stream) {
     using C = Cfg<D, FP8>;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, FP8, RAGGED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    prefill_kernel<D, FP8><<<grid, kPrefillThreads, C::SMEM_BYTES, stream>>>(p);
+    prefill_kernel<D, FP8, RAGGED><<<grid, kPrefillThreads, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- ragged schedule pass
+
+constexpr int kRBuckets = 64;
+
+// One CTA: every (sequence, query-tile pair) whose first tile has rows,
+// bucketed by the KV blocks it streams (longest first; 63 blocks or more
+// share the first bucket), each followed by its H heads (heads of one KV
+// head adjacent, so units that read the same keys run together).  Offsets or
+// lengths out of range are reported in the status word and clamped: a bad
+// query range drops the sequence, a bad key range reads no keys.
+__global__ void __launch_bounds__(1024) ragged_schedule_kernel(const RaggedSched sp, int max_pairs) {
+    __shared__ int s_bucket[kRBuckets];
+    const int t = threadIdx.x;
+    if (t < kRBuckets) s_bucket[t] = 0;
+    __syncthreads();
+    // extent of sequence s; the report is made once, by its pair-0 group
+    auto extent = [&](int s, bool report, int& qs, int& ql, int& kl, int& ks) {
+        bool bad = false;
+        const int a = __ldg(sp.cu_q + s), e = __ldg(sp.cu_q + s + 1);
+        qs = a;
+        ql = e - a;
+        if (a < 0 || e < a || e > sp.total_q || ql > sp.max_q_len) {
+            bad = true;
+            qs = 0;
+            ql = 0;
+        }
+        ks = 0;
+        if (sp.cu_k != nullptr) {
+            const int c = __ldg(sp.cu_k + s), f = __ldg(sp.cu_k + s + 1);
+            kl = f - c;
+            ks = c;
+            if (c < 0 || f < c || f > sp.kv_cap) {
+                bad = true;
+                kl = 0;
+                ks = 0;
+            }
+        } else {
+            kl = __ldg(sp.seq_lens + s);
+            if (kl < 0 || kl > sp.kv_cap) {
+                bad = true;
+                kl = kl < 0 ? 0 : sp.kv_cap;
+            }
+        }
+        if (bad && report) atomicOr(sp.status, 1u << kStatusDeviceData);
+    };
+    auto blocks = [&](int pair, int ql, int kl) {
+        int J = 0;
+        for (int tt = 0; tt < 2; ++tt) {
+            const int q0 = (2 * pair + tt) * 128, rr = ql - q0;
+            const int n = tile_blocks(q0, rr < 0 ? 0 : (rr > 128 ? 128 : rr), ql, kl, sp.causal);
+            J = n > J ? n : J;
+        }
+        return J;
+    };
+    auto bucket = [](int J) { return J >= kRBuckets - 1 ? 0 : kRBuckets - 1 - J; };
+    const int n_groups = sp.B * max_pairs;
+    for (int gi = t; gi < n_groups; gi += 1024) {
+        const int s = gi / max_pairs, pair = gi % max_pairs;
+        int qs, ql, kl, ks;
+        extent(s, pair == 0, qs, ql, kl, ks);
+        if (pair * 256 >= ql) continue;
+        atomicAdd(&s_bucket[bucket(blocks(pair, ql, kl))], sp.H);
+    }
+    __syncthreads();
+    if (t < 32) {  // exclusive scan of the 64 bucket counts (two per lane)
+        const int a = s_bucket[2 * t], c = s_bucket[2 * t + 1];
+        int x = a + c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (t >= o) x += y;
+        }
+        const int excl = x - a - c;
+        s_bucket[2 * t] = excl;
+        s_bucket[2 * t + 1] = excl + a;
+        if (t == 31) *sp.n_listed = x;
+    }
+    __syncthreads();
+    for (int gi = t; gi < n_groups; gi += 1024) {
+        const int s = gi / max_pairs, pair = gi % max_pairs;
+        int qs, ql, kl, ks;
+        extent(s, false, qs, ql, kl, ks);
+        if (pair * 256 >= ql) continue;
+        const int pos = atomicAdd(&s_bucket[bucket(blocks(pair, ql, kl))], sp.H);
+        for (int h = 0; h < sp.H; ++h) {
+            sp.units[2 * (pos + h)] = make_int4(s, pair, h, qs);
+            sp.units[2 * (pos + h) + 1] = make_int4(ql, kl, ks, 0);
+        }
+    }
 }
 
 }  // namespace
@@ -609,6 +911,21 @@ int prefill_smem_bytes(int d, bool fp8) {
     if (d == 128) return Cfg<128, false>::SMEM_BYTES;
     if (d == 64) return Cfg<64, false>::SMEM_BYTES;
     return -1;
+}
+
+size_t ragged_workspace_bytes(int B, int max_q_len, int H) {
+    const size_t pairs = (size_t)((max_q_len + 255) / 256);
+    return 256 + (size_t)B * pairs * (size_t)H * 32;
+}
+
+cudaError_t launch_ragged_prefill(int d, const RaggedSched& sp, const PrefillParams& p, int grid,
+                                  cudaStream_t stream) {
+    ragged_schedule_kernel<<<1, 1024, 0, stream>>>(sp, (sp.max_q_len + 255) / 256);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (d == 128) return launch_one<128, false, true>(p, grid, stream);
+    if (d == 64) return launch_one<64, false, true>(p, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_prefill(int d, bool fp8, const PrefillParams& p, int grid, cudaStream_t stream) {

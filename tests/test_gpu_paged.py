@@ -7,7 +7,9 @@ whose group does not divide 128, zero-length requests, prefill chunks appended
 to cached prefixes (several query tiles per request, causal and not, requests
 with no new tokens, more new tokens than keys, split key ranges merged
 across CTAs), bit-identical results under another physical page placement,
-and the device-data checks.
+and the device-data checks.  Chunks of 128 tokens or more run on the prefill
+kernel's ragged mode (two 128-token tiles of one query head per unit, keys
+gathered through the block table); shorter ones on the paged kernel.
 """
 import numpy as np
 import pytest
@@ -84,6 +86,9 @@ def test_grouped_decode_workload_full():
     (3, 4, 4, 64, 16, 40, 0, 400, 0, 200),      # 128 tokens per tile; empty requests possible
     (2, 12, 3, 128, 32, 64, 500, 900, 100, 1000),
     (1, 8, 8, 128, 64, 100, 150, 250, 5500, 6000),  # few units: split key ranges over several tiles
+    (3, 8, 2, 128, 64, 16, 1, 100, 0, 700),     # chunks under 128 tokens: the paged kernel's packed tiles
+    (2, 8, 2, 64, 8, 120, 130, 300, 0, 600),    # 8-token pages: 16 boxes per key block, d = 64
+    (2, 4, 1, 128, 256, 6, 200, 400, 100, 1000),  # pages longer than a key block
 ])
 def test_prefill_chunks(B, H, H_kv, d, page, max_pages, q_lo, q_hi, ctx_lo, ctx_hi, causal):
     p = inputs.paged_chunks(B=B, H=H, H_kv=H_kv, d=d, page_size=page, max_pages=max_pages,
@@ -146,3 +151,26 @@ def test_bad_device_data_is_reported():
     o, lse = _run(p, default_scale(128))
     o_ref, l_ref = _ref(p, default_scale(128))
     compare("gqa_after_error", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+def test_bad_device_data_is_reported_for_long_chunks():
+    """The same device-data checks on the ragged path (chunks of 128 tokens or more)."""
+    p = _gpu(inputs.paged_chunks(B=3, H=8, H_kv=2, d=128, page_size=32, max_pages=20, num_pages=70, q_lo=130,
+                                 q_hi=200, ctx_lo=0, ctx_hi=300, seed=41))
+    sl = p["seq_lens"].clone()
+    sl[1] = 100_000  # past max_pages * page_size: clamped, reported
+    attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], sl, cu_seqlens_q=p["cu_seqlens_q"],
+                   max_q_len=p["max_q_len"], causal=True)
+    with pytest.raises(attn.AttnError) as ei:
+        attn.device_status()
+    assert ei.value.status == attn.ATTN_ERR_DEVICE_DATA
+    bt = p["block_table"].clone()
+    bt[0, 0] = 70  # one past the pool: read as zeros, reported
+    attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], bt, p["seq_lens"], cu_seqlens_q=p["cu_seqlens_q"],
+                   max_q_len=p["max_q_len"], causal=True)
+    with pytest.raises(attn.AttnError) as ei:
+        attn.device_status()
+    assert ei.value.status == attn.ATTN_ERR_DEVICE_DATA
+    o, lse = _run(p, default_scale(128), causal=True, chunks=True)
+    o_ref, l_ref = _ref(p, default_scale(128), causal=True, chunks=True)
+    compare("ragged_after_error", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)

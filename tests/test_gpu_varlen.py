@@ -3,7 +3,10 @@
 Packed self-attention batches (causal and not), prefixes longer than the new
 tokens, grouped KV heads from G = 1 to 8, d = 64 and 128, empty requests,
 requests with more queries than keys, one-token queries over long keys, and
-key ranges split over several CTAs and merged.
+key ranges split over several CTAs and merged.  Launches whose longest
+request has 128 queries or more run on the prefill kernel's ragged mode
+(query tails of any length inside a tile pair); shorter ones on the paged
+kernel, and both are covered.
 """
 import numpy as np
 import pytest
@@ -42,6 +45,9 @@ def _ref(p, scale, causal):
     (4, 4, 4, 64, 0, 300, 0, 200),         # G = 1, d = 64, empty requests possible
     (3, 16, 2, 128, 1000, 1500, 0, 3000),  # G = 8, few units: key ranges split and merged
     (8, 32, 8, 128, 1, 1, 100, 3000),      # one query per request over long keys
+    (5, 8, 2, 128, 20, 100, 0, 400),       # short queries: the paged kernel's packed tiles
+    (3, 8, 2, 128, 256, 256, 0, 300),      # whole tile pairs, no ragged query tail
+    (4, 6, 3, 64, 129, 520, 0, 900),       # tails of 1..127 rows in either tile, d = 64
 ])
 def test_varlen(B, H, H_kv, d, q_lo, q_hi, ctx_lo, ctx_hi, causal):
     p = inputs.varlen_qkv(B=B, H=H, H_kv=H_kv, d=d, q_lo=q_lo, q_hi=q_hi, ctx_lo=ctx_lo, ctx_hi=ctx_hi,
