@@ -468,6 +468,27 @@ __device__ void mma_role(const PrefillParams& p, uint8_t* smem, const Bars& b, v
 
 // ---------------------------------------------------------------- softmax + epilogue
 
+// Ragged mode, once per unit: wait for V block iV and zero its row r if r >=
+// n_valid (keys past the sequence); warp-collective.  Kept out of line so the
+// softmax loop does not hold its registers.
+template <int D>
+__device__ __noinline__ bool clear_v_tail(uint8_t* smem, const Bars& b, volatile int* abort_flag, unsigned* status,
+                                          int iV, int r, int n_valid) {
+    using C = Cfg<D, false>;
+    const bool ok = __all_sync(0xffffffffu, wait_bar(&b.kv_full[iV % C::NST], (uint32_t)((iV / C::NST) & 1),
+                                                     abort_flag, status));
+    if (!ok) return false;
+    if (r >= n_valid) {
+        const uint32_t vrow = smem_u32(smem + C::OFF_KV + (iV % C::NST) * C::TILE_BYTES) + (uint32_t)(r * 128);
+#pragma unroll
+        for (int pn = 0; pn < C::NPANEL; ++pn)
+#pragma unroll
+            for (int cb = 0; cb < 128; cb += 16) st_shared_v4(vrow + (uint32_t)(pn * C::PANEL_BYTES + cb), 0u, 0u, 0u, 0u);
+    }
+    fence_async_smem();
+    return true;
+}
+
 template <int D, bool FP8, bool RAGGED>
 __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& b, volatile int* abort_flag,
                              uint32_t tmem, int t, int wq, int lane, int n_units) {
@@ -616,21 +637,9 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
                 // partial last page holds arbitrary bytes, maybe NaN, and
                 // 0 * NaN would poison P V).  The tile whose PV reads the
                 // block first clears it: tile 0 while it is active, else tile 1.
-                if (kbase + 128 > g.Nk && (t == 0 || it >= g.n[0])) {
-                    const int iV = kvb + 2 * it + 1;
-                    ok = __all_sync(0xffffffffu, wait_bar(&b.kv_full[iV % C::NST], (uint32_t)((iV / C::NST) & 1),
-                                                          abort_flag, p.status));
+                if (kbase + 128 > Nk_u && (t == 0 || it >= g.n[0])) {
+                    ok = clear_v_tail<D>(smem, b, abort_flag, p.status, kvb + 2 * it + 1, r, Nk_u - kbase);
                     if (!ok) break;
-                    if (kbase + r >= g.Nk) {
-                        const uint32_t vrow =
-                            smem_u32(smem + C::OFF_KV + (iV % C::NST) * C::TILE_BYTES) + (uint32_t)(r * 128);
-#pragma unroll
-                        for (int pn = 0; pn < C::NPANEL; ++pn)
-#pragma unroll
-                            for (int cb = 0; cb < 128; cb += 16)
-                                st_shared_v4(vrow + (uint32_t)(pn * C::PANEL_BYTES + cb), 0u, 0u, 0u, 0u);
-                    }
-                    fence_async_smem();
                 }
             }
             tmem_st_wait();
