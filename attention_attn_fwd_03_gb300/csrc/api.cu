@@ -109,6 +109,7 @@ attn_status_t prefill(const void* q, const void* k, const void* v, void* o, floa
         !make_map(&p.tm_v, v, fp8, d, Nk, BH, false) || !make_map(&p.tm_o, o, false, d, Nq, BH, true))
         return ATTN_ERR_CUDA;
     p.lse = lse;
+    p.o = static_cast<uint16_t*>(o);
     p.status = ds->status;
     p.BH = (int)BH;
     p.Nq = Nq;
