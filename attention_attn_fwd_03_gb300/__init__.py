@@ -10,8 +10,8 @@ Two levels:
     ``attn_paged_fwd``, ``attn_paged_fwd_workspace_size``,
     ``attn_varlen_fwd``, ``attn_varlen_fwd_workspace_size``, ``attn_bwd``,
     ``attn_bwd_workspace_size``, ``attn_fwd_host``, ``attn_fwd_host_workspace_size``,
-    ``attn_device_status``, ``attn_status_string``: the C entry points, same
-    names and argument order, taking raw device pointers (ints) and a stream
+    ``attn_selftest_wait_timeout``, ``attn_device_status``, ``attn_status_string``: the C entry
+    points, same names and argument order, taking raw device pointers (ints) and a stream
     handle (int).
   * ``fwd``, ``fwd_fp8``, ``paged_decode``, ``paged_fwd``, ``varlen_fwd``, ``bwd``: take torch CUDA
     tensors, allocate outputs with torch when none are given, call the C entry
@@ -93,6 +93,8 @@ def lib():
             L.attn_fwd_host_workspace_size.argtypes = [i, i, i, i, i, i, i]
             L.attn_fwd_host.restype = i
             L.attn_fwd_host.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+            L.attn_selftest_wait_timeout.restype = i
+            L.attn_selftest_wait_timeout.argtypes = [vp]
             L.attn_device_status.restype = i
             L.attn_device_status.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -172,6 +174,10 @@ def attn_fwd_host(q, k, v, n_modes, causal, o, lse, B, H, Nq, Nk, d, scale, chun
     """causal, o and lse are addresses of C arrays of n_modes entries (int, pointer, pointer)."""
     return lib().attn_fwd_host(q, k, v, n_modes, causal, o, lse, B, H, Nq, Nk, d, scale, chunk_bh, workspace,
                                workspace_bytes, stream)
+
+
+def attn_selftest_wait_timeout(stream):
+    return lib().attn_selftest_wait_timeout(stream)
 
 
 def attn_device_status(stream):

@@ -740,6 +740,13 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, int n_m
     return ATTN_OK;
 }
 
+attn_status_t attn_selftest_wait_timeout(void* stream) {
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    return from_cuda(launch_selftest_timeout(ds->status, static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t attn_device_status(void* stream) {
     DeviceState* ds = nullptr;
     attn_status_t st = device_state(&ds);

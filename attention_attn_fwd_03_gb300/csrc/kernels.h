@@ -132,6 +132,9 @@ PagedPlan paged_plan(int total_q, int max_q_len, int B, int H, int H_kv, int d, 
 int paged_smem_bytes(int d);
 cudaError_t launch_paged(int d, const PagedParams& p, int grid, cudaStream_t stream);
 
+// Failure-handling test: a bounded wait that nothing completes (selftest.cu).
+cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream);
+
 // Backward: gradients of dense attention by recomputation from the LSE.
 struct BwdParams {
     CUtensorMap tm_q;   // bf16 [BH, Nq, d], operand boxes as for prefill

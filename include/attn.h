@@ -282,6 +282,15 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, int n_m
                             void* const* o, float* const* lse, int B, int H, int Nq, int Nk, int d, float scale,
                             int chunk_bh, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Failure-handling check: launches a one-warp kernel whose bounded wait --
+ * the same wait every attention kernel uses -- is on a barrier that nothing
+ * completes.  After the wait limit (2 s) it gives up and records
+ * ATTN_ERR_TIMEOUT in the device status word, as a stalled attention kernel
+ * would; nothing faults or hangs and the context stays usable.  While the
+ * word is set the attention kernels return without work (see
+ * attn_device_status).  Errors: ATTN_ERR_CUDA if the launch fails. */
+attn_status_t attn_selftest_wait_timeout(void* stream);
+
 /* Synchronises `stream`, then reads and clears the calling device's status
  * word.  Kernels set it when a bounded internal wait gives up
  * (ATTN_ERR_TIMEOUT; the kernel then returns early and its outputs are

@@ -30,7 +30,7 @@ def test_header_declares_the_entry_points():
                                   "attn_paged_fwd", "attn_paged_fwd_workspace_size",
                                   "attn_varlen_fwd", "attn_varlen_fwd_workspace_size",
                                   "attn_bwd", "attn_bwd_workspace_size",
-                                  "attn_fwd_host", "attn_fwd_host_workspace_size",
+                                  "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_selftest_wait_timeout",
                                   "attn_device_status", "attn_status_string"])
 
 
