@@ -7,7 +7,8 @@ whose group does not divide 128, zero-length requests, prefill chunks appended
 to cached prefixes (several query tiles per request, causal and not, requests
 with no new tokens, more new tokens than keys, split key ranges merged
 across CTAs), bit-identical results under another physical page placement,
-and the device-data checks.  Chunks of 128 tokens or more run on the prefill
+and the device-data checks on both paths; the benchmark's chunk workload in its
+launch configuration on sampled rows.  Chunks of 128 tokens or more run on the prefill
 kernel's ragged mode (two 128-token tiles of one query head per unit, keys
 gathered through the block table); shorter ones on the paged kernel.
 """
@@ -174,3 +175,44 @@ def test_bad_device_data_is_reported_for_long_chunks():
     o, lse = _run(p, default_scale(128), causal=True, chunks=True)
     o_ref, l_ref = _ref(p, default_scale(128), causal=True, chunks=True)
     compare("ragged_after_error", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+def _sample(H, q_len, seed, n_random=512):
+    """Flattened (head * q_len + token) rows: the first, boundary and last rows of every head, plus random ones."""
+    g = torch.Generator().manual_seed(seed)
+    per = sorted({0, 1, 127, 128, 255, 256, q_len // 2, q_len - 2, q_len - 1} & set(range(q_len)))
+    rows = {h * q_len + i for h in range(H) for i in per}
+    rows |= set(torch.randint(0, H * q_len, (n_random,), generator=g).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def _check_sampled(name, o, lse, q, k_rows, v_rows, q_start, q_len, H, H_kv, scale, seed):
+    """Oracle on sampled rows of one request: dense [1, H, L, d] keys expanded over the G heads of a KV head."""
+    G = H // H_kv
+    qd = q[q_start:q_start + q_len].permute(1, 0, 2).unsqueeze(0).contiguous()
+    kd = k_rows.permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0).contiguous()
+    vd = v_rows.permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0).contiguous()
+    rows = _sample(H, q_len, seed)
+    o_ref, l_ref = oracle.attention(qd, kd, vd, scale, causal=True, rows=rows)
+    hh, tt = torch.from_numpy(rows // q_len), torch.from_numpy(rows % q_len)
+    o_sel = o.cpu()[q_start + tt, hh]
+    l_sel = lse.cpu()[q_start + tt, hh]
+    compare(name, o_sel, l_sel, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+def test_prefill_chunks_workload_sampled():
+    """The benchmark's chunk workload in its launch configuration (8 requests x 2048 new tokens after 6144
+    cached, 32 query heads over 8 KV heads, d = 128, 64-token pages): sampled rows of every request."""
+    p = inputs.paged_chunks(B=8, H=32, H_kv=8, d=128, page_size=64, max_pages=128, num_pages=1024, q_lo=2048,
+                            q_hi=2048, ctx_lo=6144, ctx_hi=6144, seed=0, device=DEV)
+    scale = default_scale(128)
+    o, lse = _run(p, scale, causal=True, chunks=True)
+    q, kc, vc = p["q"].cpu(), p["k_cache"].cpu(), p["v_cache"].cpu()
+    bt, sl, cu = p["block_table"].cpu(), p["seq_lens"].cpu(), p["cu_seqlens_q"].cpu()
+    for r in range(8):
+        L = int(sl[r])
+        pages = bt[r, :(L + 63) // 64].long()
+        k_rows = kc[pages].reshape(-1, 8, 128)[:L]
+        v_rows = vc[pages].reshape(-1, 8, 128)[:L]
+        _check_sampled("chunks_workload_r%d" % r, o, lse, q, k_rows, v_rows, int(cu[r]), int(cu[r + 1] - cu[r]),
+                       32, 8, scale, r)

@@ -3,7 +3,8 @@
 Packed self-attention batches (causal and not), prefixes longer than the new
 tokens, grouped KV heads from G = 1 to 8, d = 64 and 128, empty requests,
 requests with more queries than keys, one-token queries over long keys, and
-key ranges split over several CTAs and merged.  Launches whose longest
+key ranges split over several CTAs and merged; the benchmark's workload in its
+launch configuration on sampled rows.  Launches whose longest
 request has 128 queries or more run on the prefill kernel's ragged mode
 (query tails of any length inside a tile pair); shorter ones on the paged
 kernel, and both are covered.
@@ -75,3 +76,31 @@ def test_varlen_more_queries_than_keys():
     o_ref, l_ref = _ref(p, scale, True)
     assert np.isneginf(l_ref).any()
     compare("varlen_short_keys", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+def test_varlen_workload_sampled():
+    """The benchmark's varlen workload (16 causal sequences of 512..4096 tokens, 32 query heads over 8 KV
+    heads, d = 128) in its launch configuration: sampled rows of every sequence against the oracle."""
+    p = inputs.varlen_qkv(B=16, H=32, H_kv=8, d=128, q_lo=512, q_hi=4096, seed=0, device=DEV)
+    scale = default_scale(128)
+    o, lse = attn.varlen_fwd(p["q"], p["k"], p["v"], p["cu_seqlens_q"], p["cu_seqlens_k"], p["max_q_len"],
+                             p["max_k_len"], causal=True, scale=scale)
+    attn.device_status()
+    q, k, v = p["q"].cpu(), p["k"].cpu(), p["v"].cpu()
+    cq, ck = p["cu_seqlens_q"].cpu(), p["cu_seqlens_k"].cpu()
+    g = torch.Generator().manual_seed(3)
+    for r in range(16):
+        q_start, q_len = int(cq[r]), int(cq[r + 1] - cq[r])
+        k0, k1 = int(ck[r]), int(ck[r + 1])
+        G = 4
+        qd = q[q_start:q_start + q_len].permute(1, 0, 2).unsqueeze(0).contiguous()
+        kd = k[k0:k1].permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0).contiguous()
+        vd = v[k0:k1].permute(1, 0, 2).repeat_interleave(G, dim=0).unsqueeze(0).contiguous()
+        per = sorted({0, 1, 127, 128, 255, 256, q_len // 2, q_len - 1} & set(range(q_len)))
+        rows = {h * q_len + i for h in range(32) for i in per}
+        rows |= set(torch.randint(0, 32 * q_len, (256,), generator=g).tolist())
+        rows = np.array(sorted(rows), dtype=np.int64)
+        o_ref, l_ref = oracle.attention(qd, kd, vd, scale, causal=True, rows=rows)
+        hh, tt = torch.from_numpy(rows // q_len), torch.from_numpy(rows % q_len)
+        compare("varlen_workload_s%d" % r, o.cpu()[q_start + tt, hh], lse.cpu()[q_start + tt, hh], o_ref, l_ref,
+                TOL_O_BF16, TOL_LSE)
