@@ -39,6 +39,15 @@
 // when the new block max exceeds it by more than kTau; O and l share that
 // stale max so O / l is unchanged (the merge identity of section 2.2 step 4
 // holds for any common reference point), and p stays <= 2^kTau.
+//
+// Ragged mode (template flag RAGGED, bf16): variable-length sequences of
+// token-major tensors, for prefill chunks over a paged cache ("FlashAttention
+// V3 实战", section 3.2, the block-table layout) and packed variable-length
+// batches.  A schedule pass lists the units (sequence, tile pair, head),
+// longest first; the producer warp gathers each key block through the block
+// table (or the sequence's contiguous rows); the softmax clears the V rows
+// past a sequence in its last block and stores tiles that straddle a
+// sequence end row by row.  The MMA and softmax arithmetic is unchanged.
 #include <type_traits>
 
 #include "kernels.h"
