@@ -168,16 +168,21 @@ constexpr int kRaggedMinQ = 128;
 
 bool use_ragged(int max_q_len) { return max_q_len >= kRaggedMinQ; }
 
-// O map of the ragged mode over token-major [total_q, H, d]: dims (d, H,
-// total_q), box (32 elements, 1 head, 32 tokens), no swizzle.
-bool make_ragged_out_map(CUtensorMap* map, void* base, int d, long long heads, long long tokens) {
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)tokens};
-    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-    cuuint32_t box[3] = {32u, 1u, 32u};
+// Maps of the ragged mode over a token-major [rows, heads, d] tensor: dims
+// (d, rows, heads), so that a box walks rows of one head.  Operand maps: box
+// (64 elements, box_rows rows, 1 head), 128-byte swizzle; output map: box (32
+// elements, 32 rows, 1 head), no swizzle.  Zero fill outside the tensor;
+// stores are clipped.
+bool make_rows_map(CUtensorMap* map, const void* base, int d, long long heads, long long rows, int box_rows,
+                   bool out) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)heads * d * 2, (cuuint64_t)d * 2};
+    cuuint32_t box[3] = {out ? 32u : 64u, out ? 32u : (cuuint32_t)box_rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          out ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -191,8 +196,8 @@ attn_status_t ragged_prefill(DeviceState* ds, const void* q, const void* k, cons
     PrefillParams p;
     std::memset(&p, 0, sizeof p);
     const int R = block_table ? (page_size < 128 ? page_size : 128) : 128;
-    if (!make_paged_map(&p.tm_q, q, d, H, total_q, 1, 128) || !make_paged_map(&p.tm_k, k, d, H_kv, kv_rows, 1, R) ||
-        !make_paged_map(&p.tm_v, v, d, H_kv, kv_rows, 1, R) || !make_ragged_out_map(&p.tm_o, o, d, H, total_q))
+    if (!make_rows_map(&p.tm_q, q, d, H, total_q, 128, false) || !make_rows_map(&p.tm_k, k, d, H_kv, kv_rows, R, false) ||
+        !make_rows_map(&p.tm_v, v, d, H_kv, kv_rows, R, false) || !make_rows_map(&p.tm_o, o, d, H, total_q, 0, true))
         return ATTN_ERR_CUDA;
     int* n_listed = static_cast<int*>(workspace);
     int4* units = reinterpret_cast<int4*>(static_cast<char*>(workspace) + 256);

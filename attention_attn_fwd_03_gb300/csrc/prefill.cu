@@ -84,7 +84,8 @@ struct Cfg {
     // more than half an SM's shared memory: two CTAs never share one SM's
     // tensor memory (each allocates all 512 columns)
     static constexpr int SMEM_BYTES = (SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024);
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    // (+ 128 bytes of static shared memory: the producer's staged rows, ragged/paged gathers)
+    static_assert(SMEM_BYTES + 128 <= 227 * 1024, "shared memory budget");
     static_assert(D % PANEL == 0 && D % 64 == 0, "head dim");
 };
 
@@ -262,24 +263,30 @@ __device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars&
         drain_wait(&b.kv_full[idx % C::NST], (uint32_t)((idx / C::NST) & 1), p.status);
 }
 
-// Ragged mode producer (whole warp): the same stream as producer_role -- K_j,
+// Ragged mode producer (one warp): the same stream as producer_role -- K_j,
 // V_j of every KV block, the unit's Q tiles after its first block -- with
 // each 128-key block gathered from 128 / R boxes of R rows: through the block
-// table (paged keys; the lanes look up 32 page ids at a time) or from the
-// sequence's contiguous rows.  A box past the sequence's keys, or naming an
-// out-of-range page, reads the zero fill past the end of the key tensor.
+// table (paged keys) or from the sequence's contiguous rows.  A box past the
+// sequence's keys, or naming an out-of-range page, reads the zero fill past
+// the end of the key tensor.  The lanes look up the rows of 32 boxes at a
+// time (one load latency for all, staged in shared memory); lane 0 alone then
+// waits for the slots and issues the copies of those boxes' blocks.  (Lanes
+// that meet around every barrier wait -- one lane waiting, the rest at a
+// shuffle -- were measured to leave the copies late.)
 template <int D>
 __device__ void ragged_producer_role(const PrefillParams& p, uint8_t* smem, const Bars& b, volatile int* abort_flag,
                                      int lane, int n_units) {
     using C = Cfg<D, false>;
+    __shared__ int s_rows[32];
     if (lane == 0) {
         tma_prefetch_map(&p.tm_q);
         tma_prefetch_map(&p.tm_k);
         tma_prefetch_map(&p.tm_v);
     }
     const int R = p.rows_per_box;
-    const int LPB = 128 / R;  // boxes per block (1..16)
+    const int LPB = 128 / R;  // boxes per block (1..16), a divisor of 32
     const int oob = p.kv_rows;
+    const int pshift = p.block_table != nullptr ? __ffs(p.page_size) - 1 : 0;  // page_size is a power of two
     int kv_idx = 0;
     int qcnt[2] = {0, 0};
     int round_ = 0;
@@ -287,73 +294,72 @@ __device__ void ragged_producer_role(const PrefillParams& p, uint8_t* smem, cons
     for (int u = next_unit(n_units, round_); ok && u >= 0; u = next_unit(n_units, round_)) {
         const RaggedUnit g = ragged_unit(p, u);
         const int kvh = g.h / p.G;
-        int my_row = oob;
-        for (int j = 0; ok && j < g.J; ++j) {
-            const int box0 = j * LPB;
-            if ((box0 & 31) == 0) {  // lane i: the cache row of box box0 + i
-                const int bi = box0 + lane;
-                const long long key = (long long)bi * R;
+        const int32_t* bt = p.block_table != nullptr ? p.block_table + (size_t)g.s * p.max_pages : nullptr;
+        const int n_boxes = g.J * LPB;
+        for (int box0 = 0; ok && box0 < n_boxes; box0 += 32) {
+            __syncwarp();  // lane 0 has read the previous batch
+            {
+                const int key = (box0 + lane) * R;
                 int row = oob;
-                if (bi < g.J * LPB && key < g.Nk) {
-                    if (p.block_table != nullptr) {
-                        const int pg = (int)(key / p.page_size);
-                        const int id = __ldg(p.block_table + (size_t)g.s * p.max_pages + pg);
+                if (box0 + lane < n_boxes && key < g.Nk) {
+                    if (bt == nullptr) {
+                        row = g.kv_start + key;
+                    } else {
+                        const int id = __ldg(bt + (key >> pshift));
                         if (id >= 0 && id < p.num_pages)
-                            row = id * p.page_size + (int)(key % p.page_size);
+                            row = (id << pshift) + (key & (p.page_size - 1));
                         else
                             atomicOr(p.status, 1u << kStatusDeviceData);
-                    } else {
-                        row = g.kv_start + (int)key;
                     }
                 }
-                my_row = row;
+                s_rows[lane] = row;
             }
-            int rows[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) rows[i] = __shfl_sync(0xffffffffu, my_row, (box0 + (i < LPB ? i : 0)) & 31);
-#pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                if (lane == 0) {
-                    const int slot = kv_idx % C::NST, round = kv_idx / C::NST;
-                    if (round > 0) ok = wait_bar(&b.kv_empty[slot], (uint32_t)((round - 1) & 1), abort_flag, p.status);
-                    if (ok) {
+            __syncwarp();
+            if (lane == 0) {
+                const int j_end = min(g.J, (box0 + 32) / LPB);
+                for (int j = box0 / LPB; ok && j < j_end; ++j) {
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const int slot = kv_idx % C::NST, round = kv_idx / C::NST;
+                        if (round > 0 &&
+                            !wait_bar(&b.kv_empty[slot], (uint32_t)((round - 1) & 1), abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
                         bar_arrive_expect_tx(&b.kv_full[slot], C::TILE_BYTES);
                         const CUtensorMap* map = kv ? &p.tm_v : &p.tm_k;
                         uint8_t* dst = smem + C::OFF_KV + slot * C::TILE_BYTES;
-                        for (int i = 0; i < LPB; ++i)
+                        for (int i = 0; i < LPB; ++i) {
+                            const int row = s_rows[j * LPB + i - box0];
 #pragma unroll
                             for (int pn = 0; pn < C::NPANEL; ++pn)
                                 tma_load_3d(dst + pn * C::PANEL_BYTES + i * R * 128, map, &b.kv_full[slot],
-                                            pn * C::PANEL, kvh, rows[i]);
+                                            pn * C::PANEL, row, kvh);
+                        }
+                        ++kv_idx;
                     }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                ++kv_idx;
-            }
-            if (!ok || j != 0) continue;
-            // the unit's first K/V block is in flight; now its query tiles
-            if (lane == 0) {
+                    if (!ok || j != 0) continue;
+                    // the unit's first K/V block is in flight; now its query tiles
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (g.n[t] == 0) continue;
-                    if (qcnt[t] > 0 &&
-                        !wait_bar(&b.q_empty[t], (uint32_t)((qcnt[t] - 1) & 1), abort_flag, p.status)) {
-                        ok = false;
-                        break;
+                    for (int t = 0; t < 2; ++t) {
+                        if (g.n[t] == 0) continue;
+                        if (qcnt[t] > 0 &&
+                            !wait_bar(&b.q_empty[t], (uint32_t)((qcnt[t] - 1) & 1), abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        bar_arrive_expect_tx(&b.q_full[t], C::TILE_BYTES);
+#pragma unroll
+                        for (int pn = 0; pn < C::NPANEL; ++pn)
+                            tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q,
+                                        &b.q_full[t], pn * C::PANEL, g.q_start + g.q0[t], g.h);
+                        ++qcnt[t];
                     }
-                    bar_arrive_expect_tx(&b.q_full[t], C::TILE_BYTES);
-#pragma unroll
-                    for (int pn = 0; pn < C::NPANEL; ++pn)
-                        tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q, &b.q_full[t],
-                                    pn * C::PANEL, g.h, g.q_start + g.q0[t]);
-                    ++qcnt[t];
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
         }
     }
-    // Drain: every copy this warp started must land before the CTA exits.
+    // Drain: every copy lane 0 started must land before the CTA exits.
     if (lane == 0) {
         for (int t = 0; t < 2; ++t)
             if (qcnt[t] > 0) drain_wait(&b.q_full[t], (uint32_t)((qcnt[t] - 1) & 1), p.status);
@@ -716,7 +722,7 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
                 __syncwarp();
                 if (lane == 0) {
                     if (warp_rows && warp_full)
-                        tma_store_3d(&p.tm_o, ost + (nstore & 1u) * 2048u, ch * 32, g.h, g.q_start + q0 + wq * 32);
+                        tma_store_3d(&p.tm_o, ost + (nstore & 1u) * 2048u, ch * 32, g.q_start + q0 + wq * 32, g.h);
                     tma_store_commit();  // one (possibly empty) group per buffer use keeps the count exact
                 }
             }
