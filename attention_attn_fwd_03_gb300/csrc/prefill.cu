@@ -233,28 +233,27 @@ __device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars&
     bool ok = true;
     for (int u = next_unit(RAGGED ? n_units : p.n_units, round_); ok && u >= 0; u = next_unit(RAGGED ? n_units : p.n_units, round_)) {
         const UnitOf<RAGGED> g = unit_at<RAGGED>(p, u);
-        for (int j = 0; ok && j < g.J; ++j) {
+        // The unit's query tiles first, each as soon as the previous unit's
+        // last S MMA released its buffer (about when the ring frees the slot
+        // for the unit's first K block): Q comes from HBM, as no other unit
+        // reads it, so it is the longest load at a unit boundary.
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            if (g.n[t] == 0) continue;
+            if (qcnt[t] > 0 && !wait_bar(&b.q_empty[t], (uint32_t)((qcnt[t] - 1) & 1), abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            bar_arrive_expect_tx(&b.q_full[t], C::TILE_BYTES);
+#pragma unroll
+            for (int pn = 0; pn < C::NPANEL; ++pn)
+                tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q, &b.q_full[t],
+                            pn * C::PANEL, g.q0[t], g.bh);
+            ++qcnt[t];
+        }
+        for (int j = 0; ok && j < g.J; ++j)
             ok = load_kv<D, FP8>(p, smem, b, abort_flag, kv_idx, j, g.bh, false) &&
                  load_kv<D, FP8>(p, smem, b, abort_flag, kv_idx, j, g.bh, true);
-            if (!ok || j != 0) continue;
-            // the unit's first K/V block is in flight; now its query tiles,
-            // each as soon as the previous unit's last S MMA released it
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                if (g.n[t] == 0) continue;
-                if (qcnt[t] > 0 &&
-                    !wait_bar(&b.q_empty[t], (uint32_t)((qcnt[t] - 1) & 1), abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                bar_arrive_expect_tx(&b.q_full[t], C::TILE_BYTES);
-#pragma unroll
-                for (int pn = 0; pn < C::NPANEL; ++pn)
-                    tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q, &b.q_full[t],
-                                pn * C::PANEL, g.q0[t], g.bh);
-                ++qcnt[t];
-            }
-        }
     }
     // Drain: every copy this thread started must land before the CTA exits.
     for (int t = 0; t < 2; ++t)
