@@ -262,8 +262,8 @@ __device__ void producer_role(const PrefillParams& p, uint8_t* smem, const Bars&
         drain_wait(&b.kv_full[idx % C::NST], (uint32_t)((idx / C::NST) & 1), p.status);
 }
 
-// Ragged mode producer (one warp): the same stream as producer_role -- K_j,
-// V_j of every KV block, the unit's Q tiles after its first block -- with
+// Ragged mode producer (one warp): the same stream as producer_role -- the
+// unit's Q tiles, then K_j, V_j of every KV block -- with
 // each 128-key block gathered from 128 / R boxes of R rows: through the block
 // table (paged keys) or from the sequence's contiguous rows.  A box past the
 // sequence's keys, or naming an out-of-range page, reads the zero fill past
@@ -315,6 +315,24 @@ __device__ void ragged_producer_role(const PrefillParams& p, uint8_t* smem, cons
             }
             __syncwarp();
             if (lane == 0) {
+                // the unit's query tiles first (as in producer_role)
+                if (box0 == 0) {
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (g.n[t] == 0) continue;
+                        if (qcnt[t] > 0 &&
+                            !wait_bar(&b.q_empty[t], (uint32_t)((qcnt[t] - 1) & 1), abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        bar_arrive_expect_tx(&b.q_full[t], C::TILE_BYTES);
+#pragma unroll
+                        for (int pn = 0; pn < C::NPANEL; ++pn)
+                            tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q,
+                                        &b.q_full[t], pn * C::PANEL, g.q_start + g.q0[t], g.h);
+                        ++qcnt[t];
+                    }
+                }
                 const int j_end = min(g.J, (box0 + 32) / LPB);
                 for (int j = box0 / LPB; ok && j < j_end; ++j) {
                     for (int kv = 0; kv < 2; ++kv) {
@@ -335,23 +353,6 @@ __device__ void ragged_producer_role(const PrefillParams& p, uint8_t* smem, cons
                                             pn * C::PANEL, row, kvh);
                         }
                         ++kv_idx;
-                    }
-                    if (!ok || j != 0) continue;
-                    // the unit's first K/V block is in flight; now its query tiles
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-                        if (g.n[t] == 0) continue;
-                        if (qcnt[t] > 0 &&
-                            !wait_bar(&b.q_empty[t], (uint32_t)((qcnt[t] - 1) & 1), abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        bar_arrive_expect_tx(&b.q_full[t], C::TILE_BYTES);
-#pragma unroll
-                        for (int pn = 0; pn < C::NPANEL; ++pn)
-                            tma_load_3d(smem + C::OFF_Q + t * C::TILE_BYTES + pn * C::PANEL_BYTES, &p.tm_q,
-                                        &b.q_full[t], pn * C::PANEL, g.q_start + g.q0[t], g.h);
-                        ++qcnt[t];
                     }
                 }
             }
