@@ -89,6 +89,7 @@ def test_grouped_decode_workload_full():
     (1, 8, 8, 128, 64, 100, 150, 250, 5500, 6000),  # few units: split key ranges over several tiles
     (3, 8, 2, 128, 64, 16, 1, 100, 0, 700),     # chunks under 128 tokens: the paged kernel's packed tiles
     (2, 8, 2, 64, 8, 120, 130, 300, 0, 600),    # 8-token pages: 16 boxes per key block, d = 64
+    (2, 8, 2, 128, 16, 170, 128, 400, 1500, 2300),  # 16-token pages, d = 128: rows staged 4 blocks at a time
     (2, 4, 1, 128, 256, 6, 200, 400, 100, 1000),  # pages longer than a key block
 ])
 def test_prefill_chunks(B, H, H_kv, d, page, max_pages, q_lo, q_hi, ctx_lo, ctx_hi, causal):
