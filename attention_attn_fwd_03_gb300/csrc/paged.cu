@@ -451,6 +451,10 @@ __device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b
         if (u < 0) break;
         if (g.nt <= 0) continue;
         const bool row_ok = tr < g.nt;
+        // Every row of this warp is padding (a decode tile fills G of its 128 rows): its scores are
+        // not needed, so it skips their exponentials; the PV product then reads stale values in
+        // those rows, which touch only those rows of O, never stored.
+        const bool idle = wq * 32 >= g.nt * p.G;
         const int head = g.kvh * p.G + gh;
         const size_t grow = (size_t)(g.q_start + g.t0 + (row_ok ? tr : 0)) * p.H + head;  // output row
         if (g.nb == 0) {  // no visible key: O = 0, LSE = -inf (split partials: the merge sees no split)
@@ -472,69 +476,71 @@ __device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b
             const uint32_t tS = tmem + lane_off + (sblk & 1u) * 128u;
             ok = __all_sync(0xffffffffu, wait_bar(&b.s_full[sblk & 1u], (sblk >> 1) & 1u, abort_flag, p.status));
             if (!ok) break;
-            tc_fence_after();
-            uint32_t s[128];
-            tmem_ld32(tS + 0, s);
-            tmem_ld32(tS + 32, s + 32);
-            tmem_ld32(tS + 64, s + 64);
-            tmem_ld32(tS + 96, s + 96);
-            tmem_ld_wait();
-            reg_after_wait<128>(s);
-
             const long long kbase = (long long)(g.kb0 + j) * 128;
-            if (kbase + 127 > tile_limit) {  // visible columns of this row: [0, bound)
-                const long long bl = limit - kbase + 1;
-                const int bound = bl < 0 ? 0 : (bl > 128 ? 128 : (int)bl);
-#pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    if (c >= bound) s[c] = __float_as_uint(-INFINITY);
-            }
-            float mc[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float x = __uint_as_float(s[16 * q]);
-#pragma unroll
-                for (int i = 1; i < 15; i += 2)
-                    x = max3(x, __uint_as_float(s[16 * q + i]), __uint_as_float(s[16 * q + i + 1]));
-                mc[q] = fmaxf(x, __uint_as_float(s[16 * q + 15]));
-            }
-            const float mx = fmaxf(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], max3(mc[5], mc[6], mc[7])));
-            const float m_cand = mx * cs;
             float alpha = 1.f;
             bool resc = false;
-            if (m_cand > m + kTau) {
-                if (m != -INFINITY) {
-                    alpha = ex2(m - m_cand);
-                    resc = true;
-                }
-                l *= alpha;
-                m = m_cand;
-            }
-            const float m_use = (m == -INFINITY) ? 0.f : m;
-            const uint64_t cs2 = f2_pack(cs, cs);
-            const uint64_t nm2 = f2_pack(-m_use, -m_use);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+            if (!idle) {  // a warp whose rows are all padding keeps only the barrier protocol and V clearing
+                tc_fence_after();
+                uint32_t s[128];
+                tmem_ld32(tS + 0, s);
+                tmem_ld32(tS + 32, s + 32);
+                tmem_ld32(tS + 64, s + 64);
+                tmem_ld32(tS + 96, s + 96);
+                tmem_ld_wait();
+                reg_after_wait<128>(s);
+
+                if (kbase + 127 > tile_limit) {  // visible columns of this row: [0, bound)
+                    const long long bl = limit - kbase + 1;
+                    const int bound = bl < 0 ? 0 : (bl > 128 ? 128 : (int)bl);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 32 scores -> 16 packed bf16 P words per chunk
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float p0, p1;
-                    f2_unpack(
-                        f2_fma(f2_pack(__uint_as_float(s[32 * q + 2 * i]), __uint_as_float(s[32 * q + 2 * i + 1])),
-                               cs2, nm2),
-                        p0, p1);
-                    p0 = ex2(p0);
-                    p1 = ex2(p1);
-                    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                    w[i] = pack_bf16(p0, p1);
+                    for (int c = 0; c < 128; ++c)
+                        if (c >= bound) s[c] = __float_as_uint(-INFINITY);
                 }
-                tmem_st16(tS + 16 * q, w);
-            }
-            {
-                float a0, a1;
-                f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
-                l += a0 + a1;
+                float mc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float x = __uint_as_float(s[16 * q]);
+#pragma unroll
+                    for (int i = 1; i < 15; i += 2)
+                        x = max3(x, __uint_as_float(s[16 * q + i]), __uint_as_float(s[16 * q + i + 1]));
+                    mc[q] = fmaxf(x, __uint_as_float(s[16 * q + 15]));
+                }
+                const float mx = fmaxf(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], max3(mc[5], mc[6], mc[7])));
+                const float m_cand = mx * cs;
+                if (m_cand > m + kTau) {
+                    if (m != -INFINITY) {
+                        alpha = ex2(m - m_cand);
+                        resc = true;
+                    }
+                    l *= alpha;
+                    m = m_cand;
+                }
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                const uint64_t cs2 = f2_pack(cs, cs);
+                const uint64_t nm2 = f2_pack(-m_use, -m_use);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {  // 32 scores -> 16 packed bf16 P words per chunk
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float p0, p1;
+                        f2_unpack(
+                            f2_fma(f2_pack(__uint_as_float(s[32 * q + 2 * i]), __uint_as_float(s[32 * q + 2 * i + 1])),
+                                   cs2, nm2),
+                            p0, p1);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
+                        acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                        w[i] = pack_bf16(p0, p1);
+                    }
+                    tmem_st16(tS + 16 * q, w);
+                }
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
+                    l += a0 + a1;
+                }
             }
             if (j > 0) {  // O holds PV_{j-1} once its phase completed; rescale it if the max moved
                 ok = __all_sync(0xffffffffu, wait_bar(b.o_full, ocnt & 1u, abort_flag, p.status));
