@@ -1,9 +1,10 @@
 """Randomised shapes against the float64 oracle.
 
 A fixed-seed draw of sizes, head groupings, page sizes and mask modes for the
-dense prefill, prefill chunks over a paged cache (both the paged kernel and
-the prefill kernel's ragged mode, chosen by the longest chunk) and packed
-variable-length batches.  The draws mix tile-aligned and ragged lengths, tiny
+dense prefill (bf16 and FP8), prefill chunks over a paged cache (both the
+paged kernel and the prefill kernel's ragged mode, chosen by the longest
+chunk), packed variable-length batches, and decode over a paged cache
+(multi-head and grouped).  The draws mix tile-aligned and ragged lengths, tiny
 and multi-tile sequences, and requests with no new tokens, so combinations
 that the hand-picked cases do not list still meet the oracle.
 """
@@ -15,7 +16,7 @@ import attention_attn_fwd_03_gb300 as attn
 import oracle
 from attention_attn_fwd_03_gb300 import inputs
 
-from _parity import TOL_LSE, TOL_O_BF16, compare, default_scale
+from _parity import TOL_LSE, TOL_O_BF16, TOL_O_FP8, compare, default_scale
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -44,9 +45,24 @@ def _draw(kind, n, seed):
     return out
 
 
-DENSE = _draw("dense", 10, 2024)
-CHUNKS = _draw("chunks", 10, 7)
-VARLEN = _draw("varlen", 8, 99)
+DENSE = _draw("dense", 24, 2024)
+CHUNKS = _draw("chunks", 24, 7)
+VARLEN = _draw("varlen", 16, 99)
+FP8 = [dict(c, d=128) for c in _draw("dense", 8, 5)]
+
+
+def _draw_decode(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        H_kv = int(rng.choice([1, 2, 4, 8]))
+        out.append(dict(B=int(rng.integers(1, 9)), H_kv=H_kv, G=int(rng.choice([1, 2, 4, 8, 16])),
+                        d=int(rng.choice([64, 128])), page=int(rng.choice([8, 16, 32, 64, 128, 256])),
+                        lo=int(rng.integers(0, 200)), hi=int(rng.choice([300, 2000, 5000]))))
+    return out
+
+
+DECODE = _draw_decode(16, 11)
 
 
 @pytest.mark.parametrize("i", range(len(DENSE)))
@@ -93,3 +109,37 @@ def test_fuzz_varlen(i):
     o_ref, l_ref = oracle.varlen_attention(p["q"], p["k"], p["v"], p["cu_seqlens_q"], p["cu_seqlens_k"], scale,
                                            causal=c["causal"])
     compare("fuzz_varlen_%d_%s" % (i, c), o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+@pytest.mark.parametrize("i", range(len(FP8)))
+def test_fuzz_fp8(i):
+    c = FP8[i]
+    q, k, v = inputs.dense_qkv(c["B"], c["H"], c["Nq"], c["Nk"], 128, seed=4000 + i)
+    (q8, dq), (k8, dk), (v8, dv) = (inputs.fp8_quantize(t) for t in (q, k, v))
+    scale = default_scale(128)
+    o, lse = attn.fwd_fp8(q8.to(DEV), k8.to(DEV), v8.to(DEV), (dq, dk, dv), causal=c["causal"], scale=scale)
+    attn.device_status()
+    o_ref, l_ref = oracle.attention(q8, k8, v8, scale, causal=c["causal"], descales=(dq, dk, dv))
+    compare("fuzz_fp8_%d_%s" % (i, c), o, lse, o_ref, l_ref, TOL_O_FP8, TOL_LSE)
+
+
+@pytest.mark.parametrize("i", range(len(DECODE)))
+def test_fuzz_decode(i):
+    """G = 1 runs through both decode entry points (the CUDA-core split kernel and the tensor-core
+    paged kernel); G > 1 through the paged kernel."""
+    c = DECODE[i]
+    H = c["H_kv"] * c["G"]
+    max_pages = c["hi"] // c["page"] + 1
+    p = inputs.paged_kv(B=c["B"], H=H, d=c["d"], page_size=c["page"], max_pages=max_pages,
+                        num_pages=c["B"] * max_pages + 3, len_lo=c["lo"], len_hi=c["hi"], seed=5000 + i,
+                        H_kv=c["H_kv"])
+    g = {k: (v.to(DEV) if isinstance(v, torch.Tensor) and k != "used_pages" else v) for k, v in p.items()}
+    scale = default_scale(c["d"])
+    o_ref, l_ref = oracle.paged_attention(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], scale)
+    o, lse = attn.paged_fwd(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["seq_lens"], scale=scale)
+    attn.device_status()
+    compare("fuzz_decode_tc_%d_%s" % (i, c), o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+    if c["G"] == 1:
+        o2, lse2 = attn.paged_decode(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["seq_lens"], scale=scale)
+        attn.device_status()
+        compare("fuzz_decode_mha_%d_%s" % (i, c), o2, lse2, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
