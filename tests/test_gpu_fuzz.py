@@ -3,8 +3,8 @@
 A fixed-seed draw of sizes, head groupings, page sizes and mask modes for the
 dense prefill (bf16 and FP8), prefill chunks over a paged cache (both the
 paged kernel and the prefill kernel's ragged mode, chosen by the longest
-chunk), packed variable-length batches, and decode over a paged cache
-(multi-head and grouped).  The draws mix tile-aligned and ragged lengths, tiny
+chunk), packed variable-length batches, decode over a paged cache
+(multi-head and grouped) and the backward pass.  The draws mix tile-aligned and ragged lengths, tiny
 and multi-tile sequences, and requests with no new tokens, so combinations
 that the hand-picked cases do not list still meet the oracle.
 """
@@ -16,7 +16,7 @@ import attention_attn_fwd_03_gb300 as attn
 import oracle
 from attention_attn_fwd_03_gb300 import inputs
 
-from _parity import TOL_LSE, TOL_O_BF16, TOL_O_FP8, compare, default_scale
+from _parity import TOL_LSE, TOL_O_BF16, TOL_O_FP8, compare, compare_grad, default_scale
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -63,6 +63,7 @@ def _draw_decode(n, seed):
 
 
 DECODE = _draw_decode(16, 11)
+BWD = [dict(c, Nq=min(c["Nq"], 400), Nk=min(c["Nk"], 500)) for c in _draw("dense", 8, 31)]
 
 
 @pytest.mark.parametrize("i", range(len(DENSE)))
@@ -143,3 +144,19 @@ def test_fuzz_decode(i):
         o2, lse2 = attn.paged_decode(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["seq_lens"], scale=scale)
         attn.device_status()
         compare("fuzz_decode_mha_%d_%s" % (i, c), o2, lse2, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+@pytest.mark.parametrize("i", range(len(BWD)))
+def test_fuzz_bwd(i):
+    c = BWD[i]
+    q, k, v = inputs.dense_qkv(c["B"], c["H"], c["Nq"], c["Nk"], c["d"], seed=6000 + i)
+    do = torch.randn((c["B"], c["H"], c["Nq"], c["d"]), generator=torch.Generator().manual_seed(7000 + i),
+                     dtype=torch.float32).to(torch.bfloat16)
+    scale = default_scale(c["d"])
+    qg, kg, vg, dog = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = attn.fwd(qg, kg, vg, causal=c["causal"], scale=scale)
+    dq, dk, dv = attn.bwd(qg, kg, vg, o, lse, dog, causal=c["causal"], scale=scale)
+    attn.device_status()
+    ref = oracle.attention_bwd(q, k, v, do, scale, causal=c["causal"])
+    for tag, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
+        compare_grad("fuzz_bwd_%d_%s_%s" % (i, c, tag), g, r)
