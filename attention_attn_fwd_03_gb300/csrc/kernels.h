@@ -11,6 +11,8 @@ namespace attn {
 // Dense prefill.  Q/K/V are described by 3-D TMA maps over (d, rows, B*H)
 // with a (128 bytes, 128 rows) box, 128-byte swizzle and zero fill; O by a
 // map with a (32 elements, 32 rows) box and no swizzle (per-warp stores).
+// Ragged mode: the same boxes over token-major tensors, dims (d, rows, heads)
+// with a row stride of heads * d * 2 bytes; K/V boxes are R rows high.
 struct PrefillParams {
     CUtensorMap tm_q;
     CUtensorMap tm_k;
