@@ -657,6 +657,10 @@ def run_profile_case(args):
                                 q_lo=2048, q_hi=2048, ctx_lo=6144, ctx_hi=6144, seed=0, device=dev)
         fns = [lambda: attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"],
                                       cu_seqlens_q=p["cu_seqlens_q"], max_q_len=2048, causal=True)]
+    elif case == "varlen":
+        p = inputs.varlen_qkv(B=16, H=32, H_kv=8, d=128, q_lo=512, q_hi=4096, seed=0, device=dev)
+        fns = [lambda: attn.varlen_fwd(p["q"], p["k"], p["v"], p["cu_seqlens_q"], p["cu_seqlens_k"],
+                                       max_q_len=p["max_q_len"], max_k_len=p["max_k_len"], causal=True)]
     else:
         raise SystemExit("unknown --profile-case %s" % case)
     for _ in range(args.warmup):
@@ -685,7 +689,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-case", choices=["step", "long_small", "fp8", "decode_small", "gqa_decode_small",
-                                               "gqa_decode", "chunks_small", "chunks", "bwd_small"], default=None,
+                                               "gqa_decode", "chunks_small", "chunks", "bwd_small", "varlen"], default=None,
                     help="run one small workload for an ncu capture instead of the benchmark")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
