@@ -10,7 +10,8 @@ Two levels:
     ``attn_paged_fwd``, ``attn_paged_fwd_workspace_size``,
     ``attn_varlen_fwd``, ``attn_varlen_fwd_workspace_size``, ``attn_bwd``,
     ``attn_bwd_workspace_size``, ``attn_fwd_host``, ``attn_fwd_host_workspace_size``,
-    ``attn_selftest_wait_timeout``, ``attn_device_status``, ``attn_status_string``: the C entry
+    ``attn_selftest_wait_timeout``, ``attn_selftest_mma_rate``, ``attn_device_status``,
+    ``attn_status_string``: the C entry
     points, same names and argument order, taking raw device pointers (ints) and a stream
     handle (int).
   * ``fwd``, ``fwd_fp8``, ``paged_decode``, ``paged_fwd``, ``varlen_fwd``, ``bwd``: take torch CUDA
@@ -35,6 +36,9 @@ ATTN_ERR_CUDA = 3
 ATTN_ERR_WORKSPACE = 4
 ATTN_ERR_TIMEOUT = 5
 ATTN_ERR_DEVICE_DATA = 6
+
+# size of the library's fixed device scratch array used by attn_paged_decode_noalloc
+ATTN_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -95,6 +99,8 @@ def lib():
             L.attn_fwd_host.argtypes = [vp, vp, vp, i, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
             L.attn_selftest_wait_timeout.restype = i
             L.attn_selftest_wait_timeout.argtypes = [vp]
+            L.attn_selftest_mma_rate.restype = i
+            L.attn_selftest_mma_rate.argtypes = [vp, i, i, vp]
             L.attn_device_status.restype = i
             L.attn_device_status.argtypes = [vp]
             L.attn_status_string.restype = ctypes.c_char_p
@@ -114,8 +120,8 @@ def attn_fwd_fp8(q8, k8, v8, q_descale, k_descale, v_descale, o, lse, B, H, Nq, 
                               causal, stream)
 
 
-def attn_paged_decode_workspace_size(B, H, d, page_size, max_pages_per_seq):
-    return lib().attn_paged_decode_workspace_size(B, H, d, page_size, max_pages_per_seq)
+def attn_paged_decode_workspace_size(B, H, d, max_pages_per_seq, page_size):
+    return lib().attn_paged_decode_workspace_size(B, H, d, max_pages_per_seq, page_size)
 
 
 def attn_paged_decode(q, k_cache, v_cache, block_table, seq_lens, B, H, d, page_size, max_pages_per_seq,
@@ -178,6 +184,10 @@ def attn_fwd_host(q, k, v, n_modes, causal, o, lse, B, H, Nq, Nk, d, scale, chun
 
 def attn_selftest_wait_timeout(stream):
     return lib().attn_selftest_wait_timeout(stream)
+
+
+def attn_selftest_mma_rate(cycles, n_ctas, n_groups, stream):
+    return lib().attn_selftest_mma_rate(cycles, n_ctas, n_groups, stream)
 
 
 def attn_device_status(stream):
@@ -342,7 +352,7 @@ def paged_decode(q, k_cache, v_cache, block_table, seq_lens, scale=None, out=Non
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
     if lse is not None:
         _check(lse, "lse", torch.float32, (B, H))
-    ws_bytes = attn_paged_decode_workspace_size(B, H, d, page_size, max_pages)
+    ws_bytes = attn_paged_decode_workspace_size(B, H, d, max_pages, page_size)
     if ws_bytes == 0:
         raise AttnError(ATTN_ERR_UNSUPPORTED, "attn_paged_decode_workspace_size")
     if workspace is None:

@@ -17,6 +17,14 @@ namespace attn {
 // Bit k set <=> a kernel reported status code k (ATTN_ERR_TIMEOUT,
 // ATTN_ERR_DEVICE_DATA).  One word per device; cleared by attn_device_status.
 __device__ unsigned g_status_word;
+// The word as attn_device_status last took it (read and cleared in one atomic
+// step, so a bit set by a kernel on another stream meanwhile is never lost).
+__device__ unsigned g_status_taken;
+
+namespace {
+__global__ void status_take_kernel() { g_status_taken = atomicExch(&g_status_word, 0u); }
+std::mutex g_take_mu;  // one take at a time per process (g_status_taken is shared)
+}  // namespace
 
 namespace {
 
@@ -362,7 +370,7 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float
                    stream);
 }
 
-size_t attn_paged_decode_workspace_size(int B, int H, int d, int page_size, int max_pages_per_seq) {
+size_t attn_paged_decode_workspace_size(int B, int H, int d, int max_pages_per_seq, int page_size) {
     if (B < 1 || H < 1 || (d != 64 && d != 128) || page_size < 8 || page_size > 1024 || page_size % 8 != 0 ||
         max_pages_per_seq < 1)
         return 0;
@@ -752,15 +760,32 @@ attn_status_t attn_selftest_wait_timeout(void* stream) {
     return from_cuda(launch_selftest_timeout(ds->status, static_cast<cudaStream_t>(stream)));
 }
 
+attn_status_t attn_selftest_mma_rate(unsigned long long* cycles, int n_ctas, int n_groups, void* stream) {
+    if (cycles == nullptr || (reinterpret_cast<uintptr_t>(cycles) & 7u) || n_ctas < 1 || n_ctas > 65535 ||
+        n_groups < 1 || n_groups > (1 << 20))
+        return ATTN_ERR_INVALID_ARG;
+    DeviceState* ds = nullptr;
+    attn_status_t st = device_state(&ds);
+    if (st != ATTN_OK) return st;
+    return from_cuda(launch_selftest_mma_rate(n_ctas, n_groups, cycles, ds->status, static_cast<cudaStream_t>(stream)));
+}
+
 attn_status_t attn_device_status(void* stream) {
     DeviceState* ds = nullptr;
     attn_status_t st = device_state(&ds);
     if (st != ATTN_OK) return st;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ATTN_ERR_CUDA;
     unsigned word = 0;
-    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof word) != cudaSuccess) return ATTN_ERR_CUDA;
-    const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(g_take_mu);
+        status_take_kernel<<<1, 1, 0, s>>>();
+        if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+        if (cudaMemcpyFromSymbolAsync(&word, g_status_taken, sizeof word, 0, cudaMemcpyDeviceToHost, s) !=
+                cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
     if (word & (1u << ATTN_ERR_TIMEOUT)) return ATTN_ERR_TIMEOUT;
     if (word & (1u << ATTN_ERR_DEVICE_DATA)) return ATTN_ERR_DEVICE_DATA;
     return ATTN_OK;

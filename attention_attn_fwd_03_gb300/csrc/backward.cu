@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     volatile int* skip = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
 
-    if (threadIdx.x == 0) *skip = (*(volatile unsigned*)p.status != 0u) ? 1 : 0;
+    if (threadIdx.x == 0) *skip = timeout_recorded(p.status) ? 1 : 0;
     __syncthreads();
     if (*skip) return;  // an earlier launch gave up: leave the device quiet
 

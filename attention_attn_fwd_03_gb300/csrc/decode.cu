@@ -294,26 +294,30 @@ cudaError_t scratch_address(void** out) {
 }
 
 // Split plan for the fixed scratch: the default number of pages per split,
-// coarsened until the partials fit in `cap` bytes.  Returns false when even
-// one split per request does not fit.
+// or the smallest coarser one whose partials fit in `cap` bytes.  Returns
+// false when even one split per request does not fit.  Closed form: with
+// bytes(s) = roundup(B*H*s*d*4, 256) + B*H*s*8 the partials of s splits per
+// request, s_fit is the largest s with bytes(s) <= cap, and the smallest
+// pages-per-split giving at most s_fit splits is ceil(max_pages / s_fit).
 bool capped_plan(int B, int H, int d, int page_size, int max_pages, size_t cap, DecodePlan* out) {
+    const size_t rec = (size_t)B * H;  // records per split index
+    auto bytes = [&](size_t s) { return (rec * s * d * sizeof(float) + 255) / 256 * 256 + rec * s * 2 * sizeof(float); };
+    size_t s_fit = cap / (rec * (d + 2) * sizeof(float));  // ignores the 256-byte round-up: at most one too many
+    while (s_fit > 0 && bytes(s_fit) > cap) --s_fit;
+    if (s_fit < 1) return false;
     int pps = 128 / page_size;
     if (pps < 1) pps = 1;
-    for (;;) {
-        DecodePlan pl{};
-        pl.pages_per_split = pps;
-        pl.max_splits = (max_pages + pps - 1) / pps;
-        const size_t recs = (size_t)B * H * pl.max_splits;
-        pl.part_o_bytes = recs * d * sizeof(float);
-        pl.part_ml_bytes = recs * 2 * sizeof(float);
-        pl.workspace_bytes = (pl.part_o_bytes + 255) / 256 * 256 + pl.part_ml_bytes;
-        if (pl.workspace_bytes <= cap) {
-            *out = pl;
-            return true;
-        }
-        if (pps >= max_pages) return false;
-        ++pps;
-    }
+    const size_t need = ((size_t)max_pages + s_fit - 1) / s_fit;
+    if (need > (size_t)pps) pps = (int)need;
+    DecodePlan pl{};
+    pl.pages_per_split = pps;
+    pl.max_splits = (max_pages + pps - 1) / pps;
+    pl.part_o_bytes = rec * pl.max_splits * d * sizeof(float);
+    pl.part_ml_bytes = rec * pl.max_splits * 2 * sizeof(float);
+    pl.workspace_bytes = (pl.part_o_bytes + 255) / 256 * 256 + pl.part_ml_bytes;
+    if (pl.workspace_bytes > cap) return false;  // cannot happen: max_splits <= s_fit
+    *out = pl;
+    return true;
 }
 
 }  // namespace

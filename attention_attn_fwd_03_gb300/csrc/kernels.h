@@ -136,6 +136,10 @@ cudaError_t launch_paged(int d, const PagedParams& p, int grid, cudaStream_t str
 
 // Failure-handling test: a bounded wait that nothing completes (selftest.cu).
 cudaError_t launch_selftest_timeout(unsigned* status, cudaStream_t stream);
+// Tensor-core rate check: n_ctas CTAs (one per SM), each timing 4 * n_groups
+// back-to-back 128x128x16 bf16 MMAs into cycles[cta] (selftest.cu).
+cudaError_t launch_selftest_mma_rate(int n_ctas, int n_groups, unsigned long long* cycles, unsigned* status,
+                                     cudaStream_t stream);
 
 // Backward: gradients of dense attention by recomputation from the LSE.
 struct BwdParams {

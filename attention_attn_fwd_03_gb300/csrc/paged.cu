@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(kPagedThreads, 1) paged_kernel(const __grid_co
         tmem_relinquish();
     }
     griddep_launch_dependents();  // the merge kernel may be scheduled; it waits for this grid
-    if (threadIdx.x == 0) *skip = (*(volatile unsigned*)p.status != 0u) ? 1 : 0;
+    if (threadIdx.x == 0) *skip = timeout_recorded(p.status) ? 1 : 0;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

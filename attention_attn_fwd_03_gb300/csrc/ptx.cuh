@@ -74,6 +74,13 @@ __device__ __forceinline__ bool bar_try_wait_sleep(uint64_t* bar, uint32_t parit
     return ok != 0;
 }
 
+// True when some kernel of the device has recorded a timeout in the status
+// word (the only bit that makes other kernels stop: ATTN_ERR_DEVICE_DATA
+// reports bad caller data, which every kernel clamps, and cancels nothing).
+__device__ __forceinline__ bool timeout_recorded(const unsigned* status) {
+    return (*(const volatile unsigned*)status & (1u << kStatusTimeout)) != 0u;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (after flagging the CTA and the device status word) on timeout, or
 // when another role of the CTA, or another CTA, has already given up.
@@ -85,7 +92,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
         if (bar_try_wait_sleep(bar, parity, 20000u)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
-            if (*(volatile unsigned*)status != 0u) {
+            if (timeout_recorded(status)) {
                 *abort_flag = 1;
                 return false;
             }

@@ -1,30 +1,35 @@
 #!/usr/bin/env python3
 """Throughput benchmark of the GB300 attention library.
 
-One step = one pass of the prefill hot path over the batched workload
-(B=4, H=16, Nq=Nk=2048, d=128, bf16): attn_fwd non-causal, then attn_fwd
-causal, on inputs already resident in HBM.  The headline metric is TFLOPS
-with the algorithmic count 4*B*H*Nq*Nk*d per call (halved for the causal
-call).  Inputs (100 MB) are smaller than L2, so L2 is flushed (a 256 MB
-write) before every timed step, outside the timed events.
+One step = one pass of the prefill hot path over the long-context causal
+workload (B=1, H=32, Nq=Nk=32768, d=128, bf16, causal): one attn_fwd call on
+inputs already resident in HBM (805 MB of Q/K/V, larger than the 129 MB L2;
+L2 is also flushed with a 256 MB write before every timed step, outside the
+timed events).  The headline metric is TFLOPS with the algorithmic count
+4*B*H*Nq*Nk*d halved for the causal mask.
 
-Also reported in the same JSON line (timed the same way, not part of
-`value`): the long causal prefill (1x32x32768, d=128), FP8 prefill
-(2x16x8192, d=128), paged decode (64 requests, H=32, d=128, 64-token
-pages), the same decode with 32 query heads over 8 KV heads on the tensor
-cores -- both as HBM GB/s of algorithmic bytes -- and causal prefill chunks
-over a paged cache (8 requests x 2048 new tokens after 6144 cached, 32 query
-heads over 8 KV heads) and a variable-length causal batch (16 packed sequences of 512..4096
-tokens, 32 query heads over 8 KV heads) as TFLOPS of exactly counted
-visible pairs; and the backward pass of the batched workload (dQ, dK, dV),
-as TFLOPS with 2.5x the forward count.
+The line carries, for that kernel:
+  roofline     achieved FLOP/s (CUDA events per launch) against the measured
+               dense bf16 burst peak, with the DRAM traffic per launch from the
+               committed ncu capture;
+  spec_peak    the dense bf16 rate derived on this device: SM count x the
+               tensor core's measured FLOP per SM cycle (attn_selftest_mma_rate)
+               x SM clock, at the maximum and at the sampled clock;
+  e2e          the same step from page-locked host buffers through
+               attn_fwd_host (Q, K, V copied in and O, LSE copied out every
+               step, overlapped with the kernels);
+  cpu_baseline the float64 oracle on the host cores over a stratified row
+               sample of the workload (FLOPs counted exactly per visible
+               (row, key) pair), extrapolated to the whole workload.
 
-`e2e` is the same step from page-locked host buffers through attn_fwd_host:
-Q, K, V are copied in and both calls' O and LSE copied out every step, in
-chunks of (b, h) pairs whose copies in both directions overlap the kernels.
+`workloads` holds every other configuration, each with its own roofline and
+its own oracle timing: the batched prefill (4x16x2048, non-causal and
+causal), FP8 prefill (2x16x8192), paged decode (64 requests, H=32, 64-token
+pages) and its grouped-query form (32 query / 8 KV heads), prefill chunks
+over a paged cache, a variable-length batch, and the backward pass.
 
 `--impl reference` times the float64 CPU oracle (the only reference this
-method has) on a bounded row sample of the same workload.
+method has) on bounded row samples of the same workload.
 
 Multi-GPU: one process per GPU (torchrun); every rank runs its own replica of
 the step on its own inputs (weak scaling, no data-path collective); the
@@ -44,9 +49,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-B, H, N, D = 4, 16, 2048, 128
-WORKLOAD = "batched prefill B=4 H=16 Nq=Nk=2048 d=128 bf16, non-causal + causal per step"
+# the headline workload: long-context causal prefill
+B, H, N, D = 1, 32, 32768, 128
+CAUSAL = True
+WORKLOAD = "long-context causal prefill B=1 H=32 Nq=Nk=32768 d=128 bf16"
 METRIC = "attention fwd TFLOPS and % of GB300 tensor peak; paged decode HBM GB/s"
+# the batched prefill workload (reported under workloads)
+B2, H2, N2 = 4, 16, 2048
+MMA_FLOP = 2 * 128 * 128 * 16  # one 128x128x16 tcgen05.mma
 
 
 def prefill_flops(b, h, nq, nk, d, causal):
@@ -54,7 +64,7 @@ def prefill_flops(b, h, nq, nk, d, causal):
     return f / 2 if causal else f
 
 
-STEP_FLOPS = prefill_flops(B, H, N, N, D, False) + prefill_flops(B, H, N, N, D, True)
+STEP_FLOPS = prefill_flops(B, H, N, N, D, CAUSAL)
 
 
 def load_peaks():
@@ -64,9 +74,10 @@ def load_peaks():
             pk = json.load(f)
         return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
                 "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
-                "source": "measured"}
+                "sm_max_mhz": float(pk.get("sm_max_mhz", 2070.0)), "source": "measured"}
     except Exception:
-        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+                "source": "fallback"}
 
 
 def max_over_ranks(value, device=None):
@@ -195,6 +206,250 @@ class ClockSampler:
                 "samples": len(sm), "source": "nvml" if self.samples else ("nvidia-smi" if smi_sm else "none")}
 
 
+# ---------------------------------------------------------------- tensor-core rate and rooflines
+
+def measure_tensor_rate(torch, attn, dev):
+    """Dense bf16 FLOP per SM cycle of back-to-back 128x128x16 tcgen05.mma,
+    one CTA per SM (attn_selftest_mma_rate).  Returns (SMs, median, min, max)."""
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.zeros(n_sm, dtype=torch.int64, device=dev)
+    n_groups = 4096
+    st = attn.attn_selftest_mma_rate(cyc.data_ptr(), n_sm, n_groups, torch.cuda.current_stream(dev).cuda_stream)
+    if st != attn.ATTN_OK:
+        raise attn.AttnError(st, "attn_selftest_mma_rate")
+    attn.device_status()
+    rates = [4.0 * n_groups * MMA_FLOP / c for c in cyc.cpu().tolist() if c > 0]
+    if not rates:
+        raise RuntimeError("tensor-core rate check returned no timings")
+    return n_sm, statistics.median(rates), min(rates), max(rates)
+
+
+class SpecPeak:
+    """Dense bf16 peak of this device: SM count x measured FLOP per SM cycle x SM clock."""
+
+    def __init__(self, n_sm, rate, rate_lo, rate_hi, max_mhz):
+        self.n_sm, self.rate, self.lo, self.hi, self.max_mhz = n_sm, rate, rate_lo, rate_hi, max_mhz
+        self.sampled_mhz = None
+
+    def tflops(self, mhz):
+        return self.n_sm * self.rate * mhz * 1e6 / 1e12
+
+    def record(self, achieved_tflops, fp8=False):
+        """Fractions of the spec peak for a tensor-bound kernel (FP8: 2x, the nominal fp8:bf16 dense ratio)."""
+        mult = 2.0 if fp8 else 1.0
+        r = {"frac_of_spec_at_max_clock": round(achieved_tflops / (mult * self.tflops(self.max_mhz)), 4)}
+        if self.sampled_mhz:
+            r["frac_of_spec_at_sampled_clock"] = round(achieved_tflops / (mult * self.tflops(self.sampled_mhz)), 4)
+            r["achieved_flop_per_sm_cycle"] = round(achieved_tflops * 1e12 / (self.n_sm * self.sampled_mhz * 1e6), 1)
+        return r
+
+    def summary(self):
+        r = {"value": round(self.tflops(self.max_mhz), 1), "unit": "TFLOP/s", "clock_mhz": self.max_mhz,
+             "derivation": "SMs (%d, cudaGetDeviceProperties) x %.0f dense bf16 FLOP per SM cycle (measured: "
+                           "back-to-back 128x128x16 tcgen05.mma from shared memory into tensor memory, one CTA "
+                           "per SM, attn_selftest_mma_rate; per-SM range %.0f..%.0f) x SM clock"
+                           % (self.n_sm, self.rate, self.lo, self.hi),
+             "flop_per_sm_cycle": round(self.rate, 1), "sms": self.n_sm}
+        if self.sampled_mhz:
+            r["at_sampled_clock"] = {"value": round(self.tflops(self.sampled_mhz), 1),
+                                     "clock_mhz": self.sampled_mhz}
+        return r
+
+
+def tensor_roofline(achieved, peaks, kernel, traffic, fp8=False):
+    peak = peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+    src = peaks["source"] + " dense bf16 burst (kernel timed alone)" + (" x 2 (nominal fp8:bf16 dense ratio)"
+                                                                        if fp8 else "")
+    return {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel, "peak_source": src}
+
+
+def hbm_roofline(achieved_gbs, peaks, kernel, traffic):
+    return {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved_gbs / peaks["hbm_gbs"], 4), "frac_of_8TBps": round(achieved_gbs / 8000.0, 4),
+            "traffic": traffic, "kernel": kernel,
+            "peak_source": peaks["source"] + " HBM copy bandwidth (read + write bytes)"}
+
+
+# ---------------------------------------------------------------- oracle timings (CPU baselines)
+
+def _oracle_threads():
+    import oracle
+    return oracle.default_threads()
+
+
+def _baseline(value, unit, secs, sample, extra=None):
+    r = {"value": round(value, 6), "unit": unit, "cores": _oracle_threads(), "kind": "oracle", "sample": sample,
+         "seconds": round(secs, 2)}
+    if extra:
+        r.update(extra)
+    return r
+
+
+def causal_row_flops(rows, Nq, Nk, d):
+    """Exact FLOPs (4*d per visible (row, key) pair) of flattened BHSD rows under the bottom-right mask."""
+    import numpy as np
+    i = np.asarray(rows, dtype=np.int64) % Nq
+    vis = np.clip(i + 1 + (Nk - Nq), 0, Nk)
+    return 4.0 * d * float(vis.sum())
+
+
+class LongCausalOracle:
+    """The float64 oracle on row samples of the headline workload (the long
+    causal prefill); its rate calibrated once on a small random sample."""
+
+    def __init__(self, qkv=None):
+        import numpy as np
+
+        import oracle
+        from attention_attn_fwd_03_gb300 import inputs
+
+        self.np, self.oracle, self.inputs = np, oracle, inputs
+        self.q, self.k, self.v = qkv if qkv is not None else inputs.dense_qkv(B, H, N, N, D, seed=0)
+        self.scale = float(np.float32(1.0 / math.sqrt(D)))
+        self.rng = np.random.default_rng(0)
+        cal = np.sort(self.rng.choice(B * H * N, size=64, replace=False))
+        t0 = time.perf_counter()
+        oracle.attention(self.q, self.k, self.v, self.scale, causal=CAUSAL, rows=cal)
+        self.rate = causal_row_flops(cal, N, N, D) / max(time.perf_counter() - t0, 1e-6)
+
+    def _time(self, rows):
+        t0 = time.perf_counter()
+        self.oracle.attention(self.q, self.k, self.v, self.scale, causal=CAUSAL, rows=rows)
+        secs = time.perf_counter() - t0
+        return causal_row_flops(rows, N, N, D) / secs / 1e12, secs
+
+    def random_sample(self, seconds):
+        """Uniformly drawn rows worth about `seconds` of work: (TFLOPS, seconds, rows)."""
+        n = int(min(B * H * N, max(16, seconds * self.rate / (4.0 * D * N / 2))))
+        rows = self.np.sort(self.rng.choice(B * H * N, size=n, replace=False))
+        tf, secs = self._time(rows)
+        return tf, secs, n
+
+    def stratified(self, seconds):
+        """The stratified row set (first and last 128 rows, tile-boundary rows,
+        random rows) of as many heads as fit in about `seconds`, then random
+        rows over all heads for the rest of the time."""
+        np = self.np
+        per_head = self.inputs.sample_rows(1, N, n_random=0, tile=128, seed=0)
+        head_flops = causal_row_flops(per_head, N, N, D)
+        n_heads = int(max(1, min(H, 0.5 * seconds * self.rate // head_flops)))
+        strata = (np.arange(n_heads, dtype=np.int64)[:, None] * N + per_head[None, :]).ravel()
+        left = max(0.0, seconds * self.rate - n_heads * head_flops)
+        n_rand = int(min(B * H * N, max(16, left / (4.0 * D * N / 2))))
+        rows = np.unique(np.concatenate([strata, self.rng.choice(B * H * N, size=n_rand, replace=False)]))
+        tf, secs = self._time(rows)
+        full_s = STEP_FLOPS / (tf * 1e12)
+        desc = ("float64 oracle (three-pass softmax per row) on %d of %d rows of the workload: the stratified set "
+                "(rows 0-127, the last 128 rows, every tile-boundary row) of %d heads plus %d uniformly drawn rows "
+                "over all heads; FLOPs = 4*d per visible (row, key) pair; the whole workload extrapolated by its "
+                "exact visible-pair count" % (rows.size, B * H * N, n_heads, n_rand))
+        return _baseline(tf, "TFLOPS", secs, desc, {"extrapolated": True,
+                                                    "extrapolated_full_workload_seconds": round(full_s, 1)})
+
+
+def oracle_dense(qkv, causal, seconds, descales=None, label="prefill"):
+    """The oracle on a dense prefill workload: in full when it fits in about
+    `seconds` (rate estimated on a small sample), else on uniformly drawn rows."""
+    import numpy as np
+
+    import oracle
+    q, k, v = qkv
+    BH = q.shape[0] * q.shape[1]
+    Nq, Nk, d = q.shape[2], k.shape[2], q.shape[3]
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    ds = descales or (1.0, 1.0, 1.0)
+    rng = np.random.default_rng(1)
+
+    def rows_flops(rows):
+        if causal:
+            return causal_row_flops(rows, Nq, Nk, d)
+        return 4.0 * d * Nk * len(rows)
+
+    cal = np.sort(rng.choice(BH * Nq, size=min(BH * Nq, 64), replace=False))
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, scale, causal=causal, rows=cal, descales=ds)
+    rate = rows_flops(cal) / max(time.perf_counter() - t0, 1e-6)
+    total = prefill_flops(1, BH, Nq, Nk, d, False) if not causal else causal_row_flops(np.arange(Nq), Nq, Nk, d) * BH
+    if total <= 1.5 * seconds * rate:
+        rows, what = None, "all %d rows" % (BH * Nq)
+        flops = total
+    else:
+        per_row = total / (BH * Nq)
+        n = int(max(64, seconds * rate / per_row))
+        rows = np.sort(rng.choice(BH * Nq, size=n, replace=False))
+        flops, what = rows_flops(rows), "%d uniformly drawn of %d rows" % (n, BH * Nq)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, scale, causal=causal, rows=rows, descales=ds)
+    secs = time.perf_counter() - t0
+    desc = ("float64 oracle (three-pass softmax per row) on %s of the %s workload%s; FLOPs = 4*d per visible "
+            "(row, key) pair" % (what, label, " (dequantised e4m3 inputs)" if descales else ""))
+    return _baseline(flops / secs / 1e12, "TFLOPS", secs, desc)
+
+
+def _paged_subset(p, reqs, token_major_q=False):
+    """CPU copies of requests `reqs` of a paged workload with only their pages,
+    renumbered: (q, k_cache, v_cache, block_table, seq_lens, cu_seqlens_q)."""
+    import torch
+    bt = p["block_table"].cpu()
+    sl = p["seq_lens"].cpu()
+    page = p["k_cache"].shape[1]
+    ids, rows = [], []
+    new_bt = torch.full((len(reqs), bt.shape[1]), -1, dtype=torch.int32)
+    for i, r in enumerate(reqs):
+        n = (int(sl[r]) + page - 1) // page
+        new_bt[i, :n] = torch.arange(len(ids), len(ids) + n, dtype=torch.int32)
+        ids.extend(int(x) for x in bt[r, :n])
+    idx = torch.tensor(ids if ids else [0], dtype=torch.int64, device=p["k_cache"].device)
+    kc = p["k_cache"].index_select(0, idx).cpu()
+    vc = p["v_cache"].index_select(0, idx).cpu()
+    cu = None
+    if token_major_q:
+        cu_all = p["cu_seqlens_q"].cpu()
+        parts, cu_l = [], [0]
+        for r in reqs:
+            a, e = int(cu_all[r]), int(cu_all[r + 1])
+            parts.append(p["q"][a:e].cpu())
+            cu_l.append(cu_l[-1] + e - a)
+        q = torch.cat(parts)
+        cu = torch.tensor(cu_l, dtype=torch.int32)
+    else:
+        q = p["q"][torch.tensor(reqs, device=p["q"].device)].cpu()
+    return q, kc, vc, new_bt, sl[reqs].clone(), cu
+
+
+def oracle_decode(p, H_kv, n_req, label):
+    """The oracle on the first n_req requests of a paged decode workload, as
+    GB/s of the same algorithmic bytes the GPU figure counts."""
+    import numpy as np
+
+    import oracle
+    reqs = list(range(n_req))
+    q, kc, vc, bt, sl, _ = _paged_subset(p, reqs)
+    H_q, d = q.shape[1], q.shape[2]
+    page = kc.shape[1]
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    t0 = time.perf_counter()
+    if H_kv == H_q:
+        oracle.paged_decode(q, kc, vc, bt, sl, scale)
+    else:
+        oracle.paged_attention(q, kc, vc, bt, sl, scale)
+    secs = time.perf_counter() - t0
+    nbytes = decode_bytes(sl, H_q, H_kv, d, page)
+    desc = ("float64 oracle on %d of the %d requests of the %s workload (all their keys); GB/s of the "
+            "algorithmic bytes (K/V of every visible token, q, o, LSE, tables)" % (n_req, p["seq_lens"].numel(),
+                                                                                   label))
+    return _baseline(nbytes / secs / 1e9, "GB/s", secs, desc)
+
+
+def decode_bytes(seq_lens, H_q, H_kv, d, page):
+    lens = seq_lens.long().cpu()
+    B_ = lens.numel()
+    tokens = int(lens.sum())
+    n_pages = int(((lens + page - 1) // page).sum())
+    return tokens * H_kv * d * 2 * 2 + 2 * (B_ * H_q * d * 2) + B_ * H_q * 4 + n_pages * 4 + B_ * 4
+
+
 # ---------------------------------------------------------------- timing helpers
 
 def timed_launches(torch, fn, iters, flush):
@@ -231,7 +486,6 @@ def traffic_record(kernel_file, key):
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
-    import numpy as np
     import torch
 
     import attention_attn_fwd_03_gb300 as attn
@@ -250,25 +504,24 @@ def run_ours(args, rank, world, local_rank):
     def flush():
         flush_buf.fill_(1.0)
 
+    # the tensor core's dense bf16 rate per SM cycle (for the spec peak)
+    n_sm, rate, rate_lo, rate_hi = measure_tensor_rate(torch, attn, dev)
+    spec = SpecPeak(n_sm, rate, rate_lo, rate_hi, peaks["sm_max_mhz"])
+
     # inputs: seeded per rank (each rank is an independent replica)
-    q, k, v = (t.to(dev) for t in inputs.dense_qkv(B, H, N, N, D, seed=rank))
-    o_nc, l_nc = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    o_c, l_c = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    qc, kc, vc = inputs.dense_qkv(B, H, N, N, D, seed=rank)
+    q, k, v = qc.to(dev), kc.to(dev), vc.to(dev)
+    o, l = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
 
     def step():
-        attn.fwd(q, k, v, causal=False, out=o_nc, lse=l_nc)
-        attn.fwd(q, k, v, causal=True, out=o_c, lse=l_c)
+        attn.fwd(q, k, v, causal=CAUSAL, out=o, lse=l)
 
     for _ in range(args.warmup):
         flush()
         step()
     attn.device_status()
 
-    # per-launch durations of the dominant kernel (the prefill kernel, both calls)
-    nc_ms = timed_launches(torch, lambda: attn.fwd(q, k, v, causal=False, out=o_nc, lse=l_nc), 5, flush)
-    c_ms = timed_launches(torch, lambda: attn.fwd(q, k, v, causal=True, out=o_c, lse=l_c), 5, flush)
-
-    # ---- timed region: exactly K steps
+    # ---- timed region: exactly K steps, one prefill launch each
     stream = torch.cuda.current_stream()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -291,31 +544,30 @@ def run_ours(args, rank, world, local_rank):
         total_ms = max_over_ranks(total_ms, device=dev)
     ms_per_step = total_ms / args.steps
     value = STEP_FLOPS * world * args.steps / (total_ms * 1e-3) / 1e12
+    clocks = clk.summary()
+    spec.sampled_mhz = clocks.get("sm_mhz")
 
     # ---- end to end through the public API from pinned host buffers: attn_fwd_host
-    # pipelines the copies in, the kernels of both mask modes and the copies
-    # out over chunks of (b, h) pairs.  For comparison, the same step with
-    # serial copies around the device entry point.
-    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    ho = [torch.empty((B, H, N, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    hl = [torch.empty((B, H, N), dtype=torch.float32).pin_memory() for _ in range(2)]
-    host_ws = torch.empty(attn.attn_fwd_host_workspace_size(B, H, N, N, D, 2, 0), dtype=torch.uint8, device=dev)
+    # pipelines the copies in, the kernels and the copies out over chunks of
+    # (b, h) pairs.  For comparison, the same step with serial copies around
+    # the device entry point.
+    hq, hk, hv = (t.pin_memory() for t in (qc, kc, vc))
+    ho = torch.empty((B, H, N, D), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    host_ws = torch.empty(attn.attn_fwd_host_workspace_size(B, H, N, N, D, 1, 0), dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        attn.fwd_host(hq, hk, hv, causal=(False, True), out=ho, lse=hl, workspace=host_ws, synchronize=False)
+        attn.fwd_host(hq, hk, hv, causal=(CAUSAL,), out=[ho], lse=[hl], workspace=host_ws, synchronize=False)
 
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq_, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
     def serial_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        attn.fwd(dq, dk, dv, causal=False, out=o_nc, lse=l_nc)
-        attn.fwd(dq, dk, dv, causal=True, out=o_c, lse=l_c)
-        ho[0].copy_(o_nc, non_blocking=True)
-        ho[1].copy_(o_c, non_blocking=True)
-        hl[0].copy_(l_nc, non_blocking=True)
-        hl[1].copy_(l_c, non_blocking=True)
+        dq_.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        attn.fwd(dq_, dk_, dv_, causal=CAUSAL, out=o, lse=l)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(l, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
@@ -324,21 +576,25 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = timed_launches(torch, e2e_step, max(3, min(args.steps, 10)), flush)
     serial_ms = timed_launches(torch, serial_step, max(3, min(args.steps, 10)), flush)
     attn.device_status()
+    del dq_, dk_, dv_, host_ws
     h2d = 3 * q.numel() * 2
-    d2h = 2 * (o_nc.numel() * 2 + l_nc.numel() * 4)
+    d2h = o.numel() * 2 + l.numel() * 4
     e2e_val = STEP_FLOPS / (statistics.mean(e2e_ms) * 1e-3) / 1e12
 
-    # ---- dominant kernel roofline (prefill kernel: both calls of the step)
-    launch_flops = prefill_flops(B, H, N, N, D, False) + prefill_flops(B, H, N, N, D, True)
-    launch_ms = statistics.mean(nc_ms) + statistics.mean(c_ms)
-    achieved = launch_flops / (launch_ms * 1e-3) / 1e12
-    traffic_nc = traffic_record("prefill.cu", "prefill_bf16_d128_batched_noncausal")
-    traffic_c = traffic_record("prefill.cu", "prefill_bf16_d128_batched_causal")
-    traffic = (traffic_nc + traffic_c) / 2 if (traffic_nc is not None and traffic_c is not None) else None
+    # ---- dominant kernel roofline: the prefill kernel, one launch per step
+    launch_ms = statistics.mean(step_ms)
+    achieved = STEP_FLOPS / (launch_ms * 1e-3) / 1e12
+    roof = tensor_roofline(achieved, peaks, "prefill_kernel<128,bf16>",
+                           traffic_record("prefill.cu", "prefill_bf16_d128_long_causal"))
+    roof["algorithmic_bytes"] = 3 * q.numel() * 2 + o.numel() * 2 + l.numel() * 4
+    roof.update(spec.record(achieved))
 
     secondary = {}
     if not args.no_secondary:
-        secondary = run_secondary(torch, attn, inputs, dev, flush, peaks, rank)
+        del hq, hk, hv, ho, hl
+        secondary = run_secondary(torch, attn, inputs, dev, flush, peaks, spec, rank,
+                                  with_oracle=(rank == 0 and world == 1 and not args.no_cpu_baseline),
+                                  oracle_seconds=args.cpu_seconds)
 
     line = {
         "metric": METRIC,
@@ -353,25 +609,23 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1), rounded to bf16)",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D,
-                   "calls_per_step": ["non-causal", "causal"], "flops_per_step": STEP_FLOPS,
-                   "l2": "flushed (256 MB write) before every timed step, outside the timed events",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D, "causal": CAUSAL,
+                   "flops_per_step": STEP_FLOPS, "flops_convention": "4*B*H*Nq*Nk*d, halved for causal",
+                   "l2": "inputs (805 MB) larger than L2; L2 also flushed (256 MB write) before every timed step, "
+                         "outside the timed events",
                    "parallelism": "replicas (one independent workload per GPU)"},
-        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                     "traffic": traffic, "kernel": "prefill_kernel<128,bf16>",
-                     "peak_source": peaks["source"] + " dense bf16 (burst, kernel timed alone)"},
+        "roofline": roof,
+        "spec_peak": spec.summary(),
         "e2e": {"value": round(e2e_val, 3), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(statistics.mean(e2e_ms), 4),
-                "api": "attn_fwd_host (chunked copy-in / kernels / copy-out pipeline)",
+                "api": "attn_fwd_host (chunked copy-in / kernels / copy-out pipeline, pinned host buffers)",
                 "serial_copies_ms_per_step": round(statistics.mean(serial_ms), 4)},
-        "gpu_launches": 2 * args.steps,
-        "clocks": clk.summary(),
-        "per_call_ms": {"non_causal": round(statistics.mean(nc_ms), 4), "causal": round(statistics.mean(c_ms), 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
         "workloads": secondary,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(sample_seconds=args.cpu_seconds)
+        line["cpu_baseline"] = LongCausalOracle((qc, kc, vc)).stratified(args.cpu_seconds)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
@@ -379,90 +633,98 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
-def run_secondary(torch, attn, inputs, dev, flush, peaks, rank):
+def run_secondary(torch, attn, inputs, dev, flush, peaks, spec, rank, with_oracle, oracle_seconds):
+    """Every other workload: its own timing, roofline and (rank 0, one GPU) oracle timing."""
     out = {}
     reps = 5
-    # long causal prefill
-    q, k, v = (t.to(dev) for t in inputs.dense_qkv(1, 32, 32768, 32768, 128, seed=rank))
-    o, l = torch.empty_like(q), torch.empty((1, 32, 32768), dtype=torch.float32, device=dev)
-    attn.fwd(q, k, v, causal=True, out=o, lse=l)
-    ms = timed_launches(torch, lambda: attn.fwd(q, k, v, causal=True, out=o, lse=l), reps, flush)
-    f = prefill_flops(1, 32, 32768, 32768, 128, True)
-    tf = f / (statistics.mean(ms) * 1e-3) / 1e12
-    out["long_causal_prefill_1x32x32768_d128"] = {
-        "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
-        "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4)}
+    osec = max(2.0, oracle_seconds / 2)
+
+    def prefill_entry(name, ms, flops, kernel, traffic_key, oracle_fn, fp8=False, kernel_file="prefill.cu"):
+        tf = flops / (statistics.mean(ms) * 1e-3) / 1e12
+        roof = tensor_roofline(tf, peaks, kernel, traffic_record(kernel_file, traffic_key), fp8=fp8)
+        roof.update(spec.record(tf, fp8=fp8))
+        e = {"value": round(tf, 2), "unit": "TFLOPS", "ms": round(statistics.mean(ms), 4), "flops": flops,
+             "roofline": roof}
+        if with_oracle and oracle_fn is not None:
+            e["cpu_baseline"] = oracle_fn()
+        out[name] = e
+
+    # ---- batched prefill, both mask modes (the small batched workload)
+    qc, kc, vc = inputs.dense_qkv(B2, H2, N2, N2, D, seed=rank)
+    q, k, v = qc.to(dev), kc.to(dev), vc.to(dev)
+    o, l = torch.empty_like(q), torch.empty((B2, H2, N2), dtype=torch.float32, device=dev)
+    for causal in (False, True):
+        attn.fwd(q, k, v, causal=causal, out=o, lse=l)
+        ms = timed_launches(torch, lambda: attn.fwd(q, k, v, causal=causal, out=o, lse=l), reps, flush)
+        attn.device_status()
+        prefill_entry("batched_prefill_4x16x2048_d128_%s" % ("causal" if causal else "non_causal"), ms,
+                      prefill_flops(B2, H2, N2, N2, D, causal), "prefill_kernel<128,bf16>",
+                      "prefill_bf16_d128_batched_%s" % ("causal" if causal else "noncausal"),
+                      lambda: oracle_dense((qc, kc, vc), causal, osec, label="batched prefill"))
     del q, k, v, o, l
-    # FP8 prefill
-    q, k, v = inputs.dense_qkv(2, 16, 8192, 8192, 128, seed=rank)
-    (q8, dq), (k8, dk), (v8, dv) = (inputs.fp8_quantize(t) for t in (q, k, v))
-    q8, k8, v8 = q8.to(dev), k8.to(dev), v8.to(dev)
+
+    # ---- FP8 prefill
+    qc8, kc8, vc8 = inputs.dense_qkv(2, 16, 8192, 8192, 128, seed=rank)
+    (q8, dq), (k8, dk), (v8, dv) = (inputs.fp8_quantize(t) for t in (qc8, kc8, vc8))
+    del qc8, kc8, vc8
+    g8 = [t.to(dev) for t in (q8, k8, v8)]
     o, l = torch.empty((2, 16, 8192, 128), dtype=torch.bfloat16, device=dev), \
         torch.empty((2, 16, 8192), dtype=torch.float32, device=dev)
-    attn.fwd_fp8(q8, k8, v8, (dq, dk, dv), out=o, lse=l)
-    ms = timed_launches(torch, lambda: attn.fwd_fp8(q8, k8, v8, (dq, dk, dv), out=o, lse=l), reps, flush)
-    f = prefill_flops(2, 16, 8192, 8192, 128, False)
-    tf = f / (statistics.mean(ms) * 1e-3) / 1e12
-    fp8_peak = 2.0 * peaks["bf16_tflops"]
-    out["fp8_prefill_2x16x8192_d128"] = {
-        "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
-        "frac_of_fp8_peak": round(tf / fp8_peak, 4),
-        "fp8_peak_note": "measured bf16 burst x 2 (nominal fp8:bf16 dense ratio)"}
-    del q, k, v, q8, k8, v8, o, l
-    # paged decode
-    p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
-                        len_hi=8192, seed=rank, device=dev)
-    o = torch.empty_like(p["q"])
-    l = torch.empty((64, 32), dtype=torch.float32, device=dev)
-    ws = torch.empty(attn.attn_paged_decode_workspace_size(64, 32, 128, 64, 128), dtype=torch.uint8, device=dev)
-
-    def dec():
-        attn.paged_decode(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], out=o, lse=l,
-                          workspace=ws)
-    dec()
-    ms = timed_launches(torch, dec, reps, flush)
+    attn.fwd_fp8(*g8, (dq, dk, dv), out=o, lse=l)
+    ms = timed_launches(torch, lambda: attn.fwd_fp8(*g8, (dq, dk, dv), out=o, lse=l), reps, flush)
     attn.device_status()
-    total_tokens = int(p["seq_lens"].sum().item())
-    n_pages = int(((p["seq_lens"].long() + 63) // 64).sum().item())
-    alg_bytes = total_tokens * 32 * 128 * 2 * 2 + 2 * (64 * 32 * 128 * 2) + 64 * 32 * 4 + n_pages * 4 + 64 * 4
-    gbs = alg_bytes / (statistics.mean(ms) * 1e-3) / 1e9
-    out["paged_decode_64req_H32_d128_p64"] = {
-        "GBps": round(gbs, 1), "ms": round(statistics.mean(ms), 4), "algorithmic_bytes": alg_bytes,
-        "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4), "frac_of_8TBps": round(gbs / 8000.0, 4),
-        "tokens": total_tokens}
-    del p, o, l, ws
-    torch.cuda.empty_cache()
-    # grouped-query paged decode on the tensor cores: 32 query heads over 8 KV heads
-    p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
-                        len_hi=8192, seed=rank, device=dev, H_kv=8)
-    o = torch.empty_like(p["q"])
-    l = torch.empty((64, 32), dtype=torch.float32, device=dev)
-    ws = torch.empty(max(1, attn.attn_paged_fwd_workspace_size(64, 64, 1, 32, 8, 128, 64, 128)),
-                     dtype=torch.uint8, device=dev)
+    prefill_entry("fp8_prefill_2x16x8192_d128", ms, prefill_flops(2, 16, 8192, 8192, 128, False),
+                  "prefill_kernel<128,e4m3>", "prefill_fp8_d128", 
+                  lambda: oracle_dense((q8, k8, v8), False, osec, descales=(dq, dk, dv), label="FP8 prefill"),
+                  fp8=True)
+    del g8, o, l, q8, k8, v8
 
-    def gqa():
-        attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], out=o, lse=l,
-                       workspace=ws)
-    gqa()
-    ms = timed_launches(torch, gqa, reps, flush)
-    attn.device_status()
-    total_tokens = int(p["seq_lens"].sum().item())
-    n_pages = int(((p["seq_lens"].long() + 63) // 64).sum().item())
-    alg_bytes = total_tokens * 8 * 128 * 2 * 2 + 2 * (64 * 32 * 128 * 2) + 64 * 32 * 4 + n_pages * 4 + 64 * 4
-    gbs = alg_bytes / (statistics.mean(ms) * 1e-3) / 1e9
-    out["gqa_paged_decode_64req_H32_Hkv8_d128_p64"] = {
-        "GBps": round(gbs, 1), "ms": round(statistics.mean(ms), 4), "algorithmic_bytes": alg_bytes,
-        "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4), "frac_of_8TBps": round(gbs / 8000.0, 4),
-        "tokens": total_tokens}
-    del p, o, l, ws
-    torch.cuda.empty_cache()
-    # prefill chunks over a paged cache: 8 requests, 2048 new tokens after a 6144-token prefix, causal
+    # ---- paged decode (multi-head, CUDA cores) and grouped-query decode (tensor cores)
+    for H_kv, name, kernel, key in ((32, "paged_decode_64req_H32_d128_p64", "decode_split_kernel<128>",
+                                     "decode_paged"),
+                                    (8, "gqa_paged_decode_64req_H32_Hkv8_d128_p64", "paged_kernel<128>",
+                                     "paged_gqa_decode")):
+        p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
+                            len_hi=8192, seed=rank, device=dev, H_kv=H_kv)
+        o = torch.empty_like(p["q"])
+        l = torch.empty((64, 32), dtype=torch.float32, device=dev)
+        if H_kv == 32:
+            ws = torch.empty(attn.attn_paged_decode_workspace_size(64, 32, 128, 128, 64), dtype=torch.uint8,
+                             device=dev)
+
+            def fn():
+                attn.paged_decode(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], out=o,
+                                  lse=l, workspace=ws)
+            kfile = "decode.cu"
+        else:
+            ws = torch.empty(max(1, attn.attn_paged_fwd_workspace_size(64, 64, 1, 32, 8, 128, 64, 128)),
+                             dtype=torch.uint8, device=dev)
+
+            def fn():
+                attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"], out=o, lse=l,
+                               workspace=ws)
+            kfile = "paged.cu"
+        fn()
+        ms = timed_launches(torch, fn, reps, flush)
+        attn.device_status()
+        nbytes = decode_bytes(p["seq_lens"], 32, H_kv, 128, 64)
+        gbs = nbytes / (statistics.mean(ms) * 1e-3) / 1e9
+        e = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(statistics.mean(ms), 4),
+             "algorithmic_bytes": nbytes, "tokens": int(p["seq_lens"].sum().item()),
+             "roofline": hbm_roofline(gbs, peaks, kernel, traffic_record(kfile, key))}
+        if with_oracle:
+            e["cpu_baseline"] = oracle_decode(p, H_kv, 16, name)
+        out[name] = e
+        del p, o, l, ws
+        torch.cuda.empty_cache()
+
+    # ---- prefill chunks over a paged cache: 8 requests, 2048 new tokens after a 6144-token prefix, causal
     p = inputs.paged_chunks(B=8, H=32, H_kv=8, d=128, page_size=64, max_pages=128, num_pages=1024,
                             q_lo=2048, q_hi=2048, ctx_lo=6144, ctx_hi=6144, seed=rank, device=dev)
     o = torch.empty_like(p["q"])
     l = torch.empty((p["q"].shape[0], 32), dtype=torch.float32, device=dev)
-    wsb = attn.attn_paged_fwd_workspace_size(8, p["q"].shape[0], 2048, 32, 8, 128, 64, 128)
-    ws = torch.empty(max(1, wsb), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(1, attn.attn_paged_fwd_workspace_size(8, p["q"].shape[0], 2048, 32, 8, 128, 64, 128)),
+                     dtype=torch.uint8, device=dev)
 
     def chunks():
         attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"],
@@ -470,17 +732,27 @@ def run_secondary(torch, attn, inputs, dev, flush, peaks, rank):
     chunks()
     ms = timed_launches(torch, chunks, reps, flush)
     attn.device_status()
-    # exact visible (query, key) pairs: query i of a request sees 6144 + i + 1 keys
-    pairs = 8 * sum(6144 + i + 1 for i in range(2048))
-    f = 4.0 * pairs * 32 * 128
-    tf = f / (statistics.mean(ms) * 1e-3) / 1e12
-    out["paged_prefill_chunks_8x2048_over_6144_H32_Hkv8_d128_causal"] = {
-        "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
-        "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4),
-        "flops_note": "4 * d * H * visible (query, key) pairs, counted exactly"}
+    pairs = 8 * sum(6144 + i + 1 for i in range(2048))  # query i of a request sees 6144 + i + 1 keys
+
+    def chunks_oracle():
+        import numpy as np
+
+        import oracle
+        qs, kcs, vcs, bts, sls, cus = _paged_subset(p, [0], token_major_q=True)
+        t0 = time.perf_counter()
+        oracle.paged_attention(qs, kcs, vcs, bts, sls, float(np.float32(1 / math.sqrt(128))), cu_seqlens_q=cus,
+                               causal=True)
+        secs = time.perf_counter() - t0
+        f = 4.0 * (pairs / 8) * 32 * 128
+        return _baseline(f / secs / 1e12, "TFLOPS", secs,
+                         "float64 oracle on 1 of the 8 requests (all 2048 new tokens x 32 heads, its 8192 cached "
+                         "keys); FLOPs = 4*d per visible (query, key) pair")
+    prefill_entry("paged_prefill_chunks_8x2048_over_6144_H32_Hkv8_d128_causal", ms, 4.0 * pairs * 32 * 128,
+                  "prefill_kernel<128,bf16,ragged>", "ragged_prefill_chunks", chunks_oracle)
     del p, o, l, ws
     torch.cuda.empty_cache()
-    # variable-length batch prefill: 16 packed sequences of 512..4096 tokens, causal self-attention
+
+    # ---- variable-length batch prefill: 16 packed sequences of 512..4096 tokens, causal self-attention
     p = inputs.varlen_qkv(B=16, H=32, H_kv=8, d=128, q_lo=512, q_hi=4096, seed=rank, device=dev)
     o = torch.empty_like(p["q"])
     l = torch.empty((p["q"].shape[0], 32), dtype=torch.float32, device=dev)
@@ -495,19 +767,43 @@ def run_secondary(torch, attn, inputs, dev, flush, peaks, rank):
     attn.device_status()
     lens = (p["cu_seqlens_q"][1:] - p["cu_seqlens_q"][:-1]).long().cpu()
     pairs = int((lens * (lens + 1) // 2).sum())  # query i of a sequence sees i + 1 keys
-    f = 4.0 * pairs * 32 * 128
-    tf = f / (statistics.mean(ms) * 1e-3) / 1e12
-    out["varlen_prefill_16seq_512-4096_H32_Hkv8_d128_causal"] = {
-        "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4), "tokens": int(lens.sum()),
-        "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4),
-        "flops_note": "4 * d * H * visible (query, key) pairs, counted exactly"}
+
+    def varlen_oracle():
+        import numpy as np
+
+        import oracle
+        cu, cuk = p["cu_seqlens_q"].cpu(), p["cu_seqlens_k"].cpu()
+        # the shortest sequences up to about 1/16 of the batch's pairs
+        order = sorted(range(16), key=lambda r: int(lens[r]))
+        pick, got = [], 0
+        for r in order:
+            pick.append(r)
+            got += int(lens[r]) * (int(lens[r]) + 1) // 2
+            if got * 16 >= pairs:
+                break
+        pick.sort()
+        qs = torch.cat([p["q"][int(cu[r]):int(cu[r + 1])].cpu() for r in pick])
+        ks = torch.cat([p["k"][int(cuk[r]):int(cuk[r + 1])].cpu() for r in pick])
+        vs = torch.cat([p["v"][int(cuk[r]):int(cuk[r + 1])].cpu() for r in pick])
+        cs = torch.tensor([0] + list(np.cumsum([int(lens[r]) for r in pick])), dtype=torch.int32)
+        t0 = time.perf_counter()
+        oracle.varlen_attention(qs, ks, vs, cs, cs, float(np.float32(1 / math.sqrt(128))), causal=True)
+        secs = time.perf_counter() - t0
+        return _baseline(4.0 * got * 32 * 128 / secs / 1e12, "TFLOPS", secs,
+                         "float64 oracle on %d of the 16 sequences (%d tokens x 32 heads); FLOPs = 4*d per "
+                         "visible (query, key) pair" % (len(pick), sum(int(lens[r]) for r in pick)))
+    prefill_entry("varlen_prefill_16seq_512-4096_H32_Hkv8_d128_causal", ms, 4.0 * pairs * 32 * 128,
+                  "prefill_kernel<128,bf16,ragged>", "ragged_prefill_varlen", varlen_oracle)
+    out["varlen_prefill_16seq_512-4096_H32_Hkv8_d128_causal"]["tokens"] = int(lens.sum())
     del p, o, l, ws
     torch.cuda.empty_cache()
-    # backward of the batched prefill (4 x 16 x 2048, d = 128): dQ, dK, dV by recomputation
-    q, k, v = (t.to(dev) for t in inputs.dense_qkv(B, H, N, N, D, seed=rank))
+
+    # ---- backward of the batched prefill (4 x 16 x 2048, d = 128): dQ, dK, dV by recomputation
+    q, k, v = qc.to(dev), kc.to(dev), vc.to(dev)
     g = torch.Generator(device="cpu").manual_seed(rank + 1)
-    do = torch.randn((B, H, N, D), generator=g, dtype=torch.float32).to(torch.bfloat16).to(dev)
-    ws = torch.empty(attn.attn_bwd_workspace_size(B, H, N, D), dtype=torch.uint8, device=dev)
+    doc = torch.randn((B2, H2, N2, D), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    do = doc.to(dev)
+    ws = torch.empty(attn.attn_bwd_workspace_size(B2, H2, N2, D), dtype=torch.uint8, device=dev)
     grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     for causal in (False, True):
         o, l = attn.fwd(q, k, v, causal=causal)
@@ -517,75 +813,46 @@ def run_secondary(torch, attn, inputs, dev, flush, peaks, rank):
         bwd()
         ms = timed_launches(torch, bwd, reps, flush)
         attn.device_status()
-        f = 2.5 * prefill_flops(B, H, N, N, D, causal)  # five products of the forward's size
-        tf = f / (statistics.mean(ms) * 1e-3) / 1e12
-        out["backward_%dx%dx%d_d%d_%s" % (B, H, N, D, "causal" if causal else "non_causal")] = {
-            "TFLOPS": round(tf, 2), "ms": round(statistics.mean(ms), 4),
-            "frac_of_measured_bf16": round(tf / peaks["bf16_tflops"], 4),
-            "flops_note": "2.5 x the forward count (five GEMMs of the forward's size), halved for causal"}
+
+        def bwd_oracle():
+            import numpy as np
+
+            import oracle
+            sl = (slice(0, 1), slice(0, 2))  # 2 of the 64 (b, h) problems
+            t0 = time.perf_counter()
+            oracle.attention_bwd(qc[sl], kc[sl], vc[sl], doc[sl], float(np.float32(1 / math.sqrt(D))), causal=causal)
+            secs = time.perf_counter() - t0
+            f = 2.5 * prefill_flops(1, 2, N2, N2, D, causal)
+            return _baseline(f / secs / 1e12, "TFLOPS", secs,
+                             "float64 gradient oracle on 2 of the 64 (b, h) problems; FLOPs = 2.5x the forward "
+                             "count (five products of the forward's size), halved for causal")
+        prefill_entry("backward_4x16x2048_d128_%s" % ("causal" if causal else "non_causal"), ms,
+                      2.5 * prefill_flops(B2, H2, N2, N2, D, causal), "bwd_main_kernel<128>",
+                      "backward_%s" % ("causal" if causal else "noncausal"), bwd_oracle, kernel_file="backward.cu")
     del q, k, v, do, ws, grads, o, l
     torch.cuda.empty_cache()
     return out
 
 
-# ---------------------------------------------------------------- CPU oracle (reference arm and cpu_baseline)
-
-class OracleSampler:
-    """Times the float64 oracle on row samples of the step's workload (inputs
-    generated once; the per-row cost calibrated once)."""
-
-    def __init__(self):
-        import numpy as np
-
-        import oracle
-        from attention_attn_fwd_03_gb300 import inputs
-
-        self.np, self.oracle = np, oracle
-        self.q, self.k, self.v = inputs.dense_qkv(B, H, N, N, D, seed=0)
-        self.scale = float(np.float32(1.0 / math.sqrt(D)))
-        self.threads = oracle.default_threads()
-        self.rng = np.random.default_rng(0)
-        cal = np.sort(self.rng.choice(B * H * N, size=256, replace=False))
-        t0 = time.perf_counter()
-        oracle.attention(self.q, self.k, self.v, self.scale, causal=False, rows=cal, nthreads=self.threads)
-        self.per_row = max((time.perf_counter() - t0) / 256, 1e-7)
-
-    def run(self, seconds):
-        """One timed sample of about `seconds` of CPU work: the same rows, non-causal
-        then causal.  Returns (TFLOPS-equivalent, seconds, description)."""
-        np = self.np
-        n = int(min(B * H * N, max(256, seconds / 1.5 / self.per_row)))
-        rows = np.sort(self.rng.choice(B * H * N, size=n, replace=False))
-        t0 = time.perf_counter()
-        self.oracle.attention(self.q, self.k, self.v, self.scale, causal=False, rows=rows, nthreads=self.threads)
-        self.oracle.attention(self.q, self.k, self.v, self.scale, causal=True, rows=rows, nthreads=self.threads)
-        secs = time.perf_counter() - t0
-        flops = 4.0 * D * N * n + 4.0 * D * float(np.sum(rows % N + 1))
-        desc = ("float64 oracle (three-pass softmax per row) on %d of %d rows, non-causal and causal, "
-                "of the step's workload; FLOPs = 4*d per visible (row, key) pair" % (n, B * H * N))
-        return flops / secs / 1e12, secs, desc
-
-
-def cpu_baseline(sample_seconds):
-    sampler = OracleSampler()
-    val, secs, desc = sampler.run(sample_seconds)
-    return {"value": round(val, 6), "unit": "TFLOPS", "cores": sampler.threads, "kind": "oracle",
-            "sample": desc, "seconds": round(secs, 2)}
-
+# ---------------------------------------------------------------- reference arm
 
 def run_reference(args, rank, world):
+    """The float64 oracle, as it stands, on bounded row samples of the headline
+    workload; rank 0 only."""
     if rank != 0:
         return
-    sampler = OracleSampler()
+    sampler = LongCausalOracle()
     per_step = max(0.2, args.cpu_seconds / max(1, args.steps))
     for _ in range(args.warmup):
-        sampler.run(per_step / 2)
-    vals, secs, desc = [], [], ""
+        sampler.random_sample(per_step / 2)
+    vals, secs, n = [], [], 0
     for _ in range(args.steps):
-        v, s, desc = sampler.run(per_step)
+        v, s, n = sampler.random_sample(per_step)
         vals.append(v)
         secs.append(s)
     value = statistics.mean(vals)
+    desc = ("float64 oracle (three-pass softmax per row) on %d uniformly drawn of the %d rows of the workload per "
+            "step; FLOPs = 4*d per visible (row, key) pair" % (n, B * H * N))
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -600,8 +867,8 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1), rounded to bf16)",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": sampler.threads, "kind": "oracle",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D, "causal": CAUSAL},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": _oracle_threads(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -619,8 +886,11 @@ def run_profile_case(args):
     torch.cuda.set_device(dev)
     attn.lib()
     case = args.profile_case
-    if case == "step":
+    if case == "step":  # the headline step (long causal prefill), full size
         q, k, v = (t.to(dev) for t in inputs.dense_qkv(B, H, N, N, D, seed=0))
+        fns = [lambda: attn.fwd(q, k, v, causal=CAUSAL)]
+    elif case == "batched":
+        q, k, v = (t.to(dev) for t in inputs.dense_qkv(B2, H2, N2, N2, D, seed=0))
         fns = [lambda: attn.fwd(q, k, v, causal=False), lambda: attn.fwd(q, k, v, causal=True)]
     elif case == "long_small":
         q, k, v = (t.to(dev) for t in inputs.dense_qkv(1, 4, 32768, 32768, 128, seed=0))
@@ -688,7 +958,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["step", "long_small", "fp8", "decode_small", "gqa_decode_small",
+    ap.add_argument("--profile-case", choices=["step", "batched", "long_small", "fp8", "decode_small", "gqa_decode_small",
                                                "gqa_decode", "chunks_small", "chunks", "bwd_small", "varlen"], default=None,
                     help="run one small workload for an ncu capture instead of the benchmark")
     args = ap.parse_args()

@@ -87,8 +87,11 @@ attn_status_t attn_fwd_fp8(const void* q8, const void* k8, const void* v8,
 
 /* Bytes of device workspace attn_paged_decode needs for these sizes
  * (0 on invalid sizes).  The workspace holds the per-split partial results
- * (unnormalised O, m, l) that the merge step combines. */
-size_t attn_paged_decode_workspace_size(int B, int H, int d, int page_size, int max_pages_per_seq);
+ * (unnormalised O, m, l) that the merge step combines.
+ * NOTE the argument order: max_pages_per_seq comes BEFORE page_size here,
+ * the reverse of attn_paged_decode's own (..., page_size, max_pages_per_seq,
+ * ...).  Both are int, so swapping them is not caught by the compiler. */
+size_t attn_paged_decode_workspace_size(int B, int H, int d, int max_pages_per_seq, int page_size);
 
 /* One-token decode over a paged KV cache ("FlashAttention V3 实战", section
  * 3.2: vLLM/SGLang-style page tables).  Each request's keys are split into
@@ -102,7 +105,7 @@ size_t attn_paged_decode_workspace_size(int B, int H, int d, int page_size, int 
  *     key t lives at cache[block_table[r][t / page_size]][t % page_size]
  *   o: bf16 [B, H, d]; lse: fp32 [B, H] or NULL
  *   workspace: device buffer of at least
- *     attn_paged_decode_workspace_size(B, H, d, page_size, max_pages_per_seq)
+ *     attn_paged_decode_workspace_size(B, H, d, max_pages_per_seq, page_size)
  *     bytes, owned by the caller, contents need no initialisation.
  *   d in {64, 128}; page_size a multiple of 8 in [8, 1024].
  * Device-side data (seq_lens, block_table) is the caller's contract: a
@@ -287,18 +290,41 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, int n_m
  * completes.  After the wait limit (2 s) it gives up and records
  * ATTN_ERR_TIMEOUT in the device status word, as a stalled attention kernel
  * would; nothing faults or hangs and the context stays usable.  While the
- * word is set the attention kernels return without work (see
+ * timeout is recorded the attention kernels return without work (see
  * attn_device_status).  Errors: ATTN_ERR_CUDA if the launch fails. */
 attn_status_t attn_selftest_wait_timeout(void* stream);
 
+/* Dense tensor-core rate check (no counterpart on the attention pages: the
+ * denominator of the prefill roofline, measured rather than quoted).
+ * Launches n_ctas CTAs of 128 threads, each large enough in shared memory to
+ * have an SM to itself (launch one per SM).  One thread per CTA issues
+ * 4 * n_groups back-to-back tcgen05.mma of M = N = 128, K = 16, bf16
+ * operands from shared memory, fp32 accumulation into tensor memory (the
+ * pattern of S = Q K^T), and writes the SM cycles they took (clock64, from
+ * the first issue to completion) to cycles[cta].  Each MMA is
+ * 2 * 128 * 128 * 16 FLOP, so FLOP per SM cycle = 524288 * n_groups /
+ * cycles[cta]; x SM count x SM clock = the device's dense bf16 rate.
+ *   cycles: DEVICE array of n_ctas uint64, 8-byte aligned (written; 0 for a
+ *   CTA whose bounded wait gave up, which also sets ATTN_ERR_TIMEOUT).
+ *   1 <= n_ctas <= 65535, 1 <= n_groups <= 2^20.
+ * Errors: ATTN_ERR_INVALID_ARG before the launch; ATTN_ERR_CUDA if it fails. */
+attn_status_t attn_selftest_mma_rate(unsigned long long* cycles, int n_ctas, int n_groups, void* stream);
+
 /* Synchronises `stream`, then reads and clears the calling device's status
- * word.  Kernels set it when a bounded internal wait gives up
+ * word in one atomic step (a one-thread kernel on `stream`; a bit another
+ * stream's kernel sets meanwhile is kept for the next call, never lost).
+ * Kernels set the word when a bounded internal wait gives up
  * (ATTN_ERR_TIMEOUT; the kernel then returns early and its outputs are
- * undefined) or when paged-decode device data is out of range
- * (ATTN_ERR_DEVICE_DATA).  While the word is set, the attn_fwd, attn_fwd_fp8
- * and attn_paged_fwd kernels return without work, so check it after any
- * call whose result matters.
- * Returns ATTN_OK, one of those two codes, or ATTN_ERR_CUDA. */
+ * undefined) or when device-side lengths, offsets or page ids are out of
+ * range (ATTN_ERR_DEVICE_DATA; the kernel clamps them, carries on, and the
+ * call's results are undefined).
+ * While a TIMEOUT is recorded, every attention kernel of the device returns
+ * without work -- those launched later, and those already running on any
+ * stream, at their next internal wait -- so a stalled device goes quiet.
+ * DEVICE_DATA cancels nothing: it only reports the call that found the bad
+ * data.  Check the word after any call whose result matters.
+ * Returns ATTN_OK, one of those two codes (TIMEOUT first when both are set),
+ * or ATTN_ERR_CUDA. */
 attn_status_t attn_device_status(void* stream);
 
 /* Static English description of a status code (never NULL). */

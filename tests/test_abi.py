@@ -31,7 +31,7 @@ def test_header_declares_the_entry_points():
                                   "attn_varlen_fwd", "attn_varlen_fwd_workspace_size",
                                   "attn_bwd", "attn_bwd_workspace_size",
                                   "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_selftest_wait_timeout",
-                                  "attn_device_status", "attn_status_string"])
+                                  "attn_selftest_mma_rate", "attn_device_status", "attn_status_string"])
 
 
 def test_every_declared_symbol_is_exported(L):
@@ -87,16 +87,20 @@ def test_fp8_validation(L):
 
 
 def test_workspace_size_query(L):
-    ws = attn.attn_paged_decode_workspace_size(64, 32, 128, 64, 128)
+    # argument order (B, H, d, max_pages_per_seq, page_size)
+    ws = attn.attn_paged_decode_workspace_size(64, 32, 128, 128, 64)
     assert ws >= 64 * 32 * 130 * 4  # at least one (O, m, l) record per (request, head)
-    assert attn.attn_paged_decode_workspace_size(64, 32, 128, 64, 256) > ws
-    assert attn.attn_paged_decode_workspace_size(64, 32, 96, 64, 128) == 0
-    assert attn.attn_paged_decode_workspace_size(64, 32, 128, 12, 128) == 0
-    assert attn.attn_paged_decode_workspace_size(0, 32, 128, 64, 128) == 0
+    assert attn.attn_paged_decode_workspace_size(64, 32, 128, 256, 64) > ws
+    assert attn.attn_paged_decode_workspace_size(64, 32, 96, 128, 64) == 0
+    assert attn.attn_paged_decode_workspace_size(64, 32, 128, 128, 12) == 0
+    assert attn.attn_paged_decode_workspace_size(0, 32, 128, 128, 64) == 0
+    # page_size is validated as a page size, max_pages_per_seq as a count:
+    # 12 pages of 64 is valid, 64 pages of 12 is not
+    assert attn.attn_paged_decode_workspace_size(64, 32, 128, 12, 64) > 0
 
 
 def test_paged_decode_validation(L):
-    ws = attn.attn_paged_decode_workspace_size(4, 2, 128, 64, 8)
+    ws = attn.attn_paged_decode_workspace_size(4, 2, 128, 8, 64)
     base = dict(q=FAKE, k_cache=FAKE, v_cache=FAKE, block_table=FAKE, seq_lens=FAKE, B=4, H=2, d=128,
                 page_size=64, max_pages_per_seq=8, num_pages=32, scale=0.088, o=FAKE, lse=None,
                 workspace=FAKE, workspace_bytes=ws, stream=None)
@@ -213,3 +217,19 @@ def test_fwd_host_workspace_and_validation(L):
     assert attn.attn_fwd_host(**dict(base, causal=ctypes.addressof(bad_modes))) == attn.ATTN_ERR_INVALID_ARG
     no_out = (ctypes.c_void_p * 2)(FAKE, None)
     assert attn.attn_fwd_host(**dict(base, o=ctypes.addressof(no_out))) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_noalloc_scratch_size_matches_header():
+    """The binding's copy of ATTN_NOALLOC_SCRATCH_BYTES is the header's."""
+    with open(os.path.join(ROOT, "include", "attn.h")) as f:
+        m = re.search(r"#define ATTN_NOALLOC_SCRATCH_BYTES \((\d+)u \* (\d+)u \* (\d+)u\)", f.read())
+    assert m is not None
+    assert attn.ATTN_NOALLOC_SCRATCH_BYTES == int(m.group(1)) * int(m.group(2)) * int(m.group(3))
+
+
+def test_selftest_mma_rate_validation(L):
+    assert attn.attn_selftest_mma_rate(None, 1, 1, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_selftest_mma_rate(FAKE + 4, 1, 1, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_selftest_mma_rate(FAKE, 0, 1, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_selftest_mma_rate(FAKE, 1, 0, None) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_selftest_mma_rate(FAKE, 1, (1 << 20) + 1, None) == attn.ATTN_ERR_INVALID_ARG

@@ -1,8 +1,9 @@
 """bf16 prefill parity: the CUDA path through the C ABI against the float64 oracle.
 
-Covers the tiny (1x1x256x256, d=64) and batched (4x16x2048x2048, d=128,
-non-causal and causal) workloads in full, the long causal workload
-(1x32x32768x32768, d=128) on a stratified row sample, and edge cases:
+Covers the tiny (1x1x256x256, d=64), batched (4x16x2048x2048, d=128,
+non-causal and causal) and long causal (1x32x32768x32768, d=128) workloads
+in full -- the long one also on a stratified row sample, which fails fast --
+and edge cases:
 ragged tails, a single row/key, Nq != Nk in both directions with the
 bottom-right causal mask (including rows that see no key), large-magnitude
 inputs, determinism, and guard bands around the outputs.
@@ -82,6 +83,17 @@ def test_prefill_long_causal_sampled():
     ridx = torch.from_numpy(rows).to(DEV)
     compare("prefill_long_causal_sampled", o.reshape(-1, d).index_select(0, ridx),
             lse.reshape(-1).index_select(0, ridx), o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+def test_prefill_long_causal_full():
+    """B=1, H=32, N=32768, d=128, causal: every output element of the
+    1,048,576 rows (about 8.8 TFLOP of float64 oracle work)."""
+    B, H, N, d = 1, 32, 32768, 128
+    q, k, v = inputs.dense_qkv(B, H, N, N, d, seed=0)
+    scale = default_scale(d)
+    o, lse = _run(q, k, v, True, scale)
+    o_ref, l_ref = oracle.attention(q, k, v, scale, causal=True)
+    compare("prefill_long_causal_full", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
 
 
 @pytest.mark.parametrize("mult", [4.0, 8.0])

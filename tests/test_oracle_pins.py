@@ -602,3 +602,15 @@ def test_backward_bf16_inputs_are_decoded_exactly():
                              0.25, causal=True)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def test_fp8_dequantised_inputs_equal_the_oracle_decoder():
+    """The widening the full FP8 workload check does in torch (e4m3 code to
+    float64, times the descale, in float64) equals the oracle's own e4m3
+    decode times the descale, for every code."""
+    codes = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn)
+    finite = torch.isfinite(codes.to(torch.float32))
+    desc = 0.0123456789
+    ours = (codes.to(torch.float64) * desc)[finite].numpy()
+    theirs = (oracle.decode_elems(codes) * desc)[finite.numpy()]
+    assert (ours == theirs).all()
