@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB_NAME = "libattn_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["api.cu", "prefill.cu", "decode.cu", "paged.cu", "backward.cu", "selftest.cu"]
+SOURCES = ["api.cu", "prefill.cu", "prefill_sp.cu", "decode.cu", "paged.cu", "backward.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

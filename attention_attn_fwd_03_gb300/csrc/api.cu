@@ -92,6 +92,40 @@ bool make_map(CUtensorMap* map, const void* base, bool fp8, int d, long long row
     return r == CUDA_SUCCESS;
 }
 
+// The decoupled prefill kernel (prefill_sp.cu) is the faster one when a
+// unit -- two 128-row query tiles -- streams many KV blocks; with short rows
+// its unit boundaries, where both tiles end together, cost more than its
+// overlap gains, and the turn-based kernel (prefill.cu) is faster.  Measured
+// on GB300 (bf16 d = 128): 16 blocks per unit (4x16x2048, non-causal) favour
+// the turn-based kernel by 12%; 64 (FP8 2x16x8192) and ~128 (causal
+// 1x32x32768) favour the decoupled one by 4% and 7%.
+constexpr double kSpMinMeanBlocks = 48.0;
+
+// Mean number of KV blocks a unit streams (the longer of its two tiles).
+double mean_unit_blocks(int Nq, int Nk, int causal) {
+    const long long kv_blocks = ((long long)Nk + 127) / 128;
+    if (!causal) return (double)kv_blocks;
+    const long long pairs = ((long long)Nq + 255) / 256;
+    auto tile = [&](long long q0) -> long long {  // blocks of tile [q0, q0 + 128) clipped to Nq
+        if (q0 >= Nq) return 0;
+        const long long rows = (Nq - q0) < 128 ? (Nq - q0) : 128;
+        const long long last_key = q0 + rows - 1 + (Nk - Nq);
+        if (last_key < 0) return 0;
+        const long long nb = last_key / 128 + 1;
+        return nb < kv_blocks ? nb : kv_blocks;
+    };
+    // J of pair i grows with i; sum it exactly for up to 2^16 pairs, else
+    // take 4096 evenly spaced pairs
+    const long long step = pairs <= 65536 ? 1 : pairs / 4096;
+    double sum = 0.0;
+    long long n = 0;
+    for (long long i = 0; i < pairs; i += step, ++n) {
+        const long long a = tile(2 * i * 128), b = tile((2 * i + 1) * 128);
+        sum += (double)(a > b ? a : b);
+    }
+    return n ? sum / (double)n : 0.0;
+}
+
 attn_status_t prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                       int Nk, int d, float scale, int causal, bool fp8, float dq, float dk, float dv,
                       void* stream) {
@@ -131,7 +165,9 @@ attn_status_t prefill(const void* q, const void* k, const void* v, void* o, floa
     if (units > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     p.n_units = (int)units;
     const int grid = units < ds->sm_count ? (int)units : ds->sm_count;  // persistent: one CTA per SM
-    return from_cuda(launch_prefill(d, fp8, p, grid, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (mean_unit_blocks(Nq, Nk, causal) >= kSpMinMeanBlocks) return from_cuda(launch_prefill_sp(d, fp8, p, grid, s));
+    return from_cuda(launch_prefill(d, fp8, p, grid, s));
 }
 
 bool pow2_in(int x, int lo, int hi) { return x >= lo && x <= hi && (x & (x - 1)) == 0; }

@@ -36,11 +36,17 @@ struct PrefillParams {
     int kv_rows;             // rows of the key tensor: the first row past it reads as zeros
 };
 
-constexpr int kPrefillThreads = 352;  // 2 MMA issuer warps + TMA warp + 2 softmax warpgroups
+constexpr int kPrefillThreads = 352;  // 2 MMA issuer warps + TMA warp + 2 softmax warpgroups (both designs)
 
+// Turn-based prefill kernel (prefill.cu): P overwrites S in tensor memory.
 int prefill_smem_bytes(int d, bool fp8);
 // grid = number of persistent CTAs (at most one per SM and at most n_units)
 cudaError_t launch_prefill(int d, bool fp8, const PrefillParams& p, int grid, cudaStream_t stream);
+// Decoupled prefill kernel (prefill_sp.cu): P in shared memory, S of the next
+// block computed during the softmax; the faster one for long rows.  Dense
+// (non-ragged) launches only; same parameters and grid rule.
+int prefill_sp_smem_bytes(int d, bool fp8);
+cudaError_t launch_prefill_sp(int d, bool fp8, const PrefillParams& p, int grid, cudaStream_t stream);
 
 // Ragged prefill: the prefill kernel over variable-length sequences of
 // token-major tensors (q, o [total_q, H, d]; keys [rows, H_kv, d], contiguous

@@ -6,8 +6,11 @@
 //   128 bytes of the head dim (64 bf16 or 128 e4m3 elements); a panel is
 //   128 rows x 128 B = 16 KB and panel p of a tile starts p * 16 KB in.
 //   V tiles: the same bytes read MN-major (the head dim is the N axis).
-//   S and P: tensor memory, 128 lanes x 128 columns; P overwrites S (bf16
-//   pairs or e4m3 quadruples per 32-bit column).
+//   S: tensor memory, 128 lanes x 128 columns.  P, in the paged kernel and
+//   the turn-based prefill kernel, overwrites S in tensor memory (bf16 pairs
+//   or e4m3 quadruples per 32-bit column); in the decoupled prefill kernel P
+//   is a shared-memory tile laid out like Q (128 rows, K-major, 128-byte
+//   swizzle, panels of 128 bytes of keys).
 #pragma once
 
 #include "ptx.cuh"
@@ -55,6 +58,22 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint6
         mma4_ts<PC, 2 * PC, 3 * PC, VB, 2 * VB, 3 * VB, FP8>(o_tmem, p_tmem + (uint32_t)(4 * g * PC),
                                                            b0 + (uint64_t)(4 * g * VB), C::ID_PV,
                                                            (accumulate || g > 0) ? 1u : 0u);
+}
+
+// O += P V with P in shared memory (the decoupled prefill kernel): A = P, K-major like
+// a Q tile (panels of 128 bytes of keys, PANEL_BYTES apart), B = V MN-major.
+// Step s covers keys s * MMA_K ..: A advances (s % 4) * 32 bytes within a
+// panel and a panel every 4 steps; B advances s * MMA_K rows.
+template <int D, bool FP8>
+__device__ __forceinline__ void issue_pv_ss(uint32_t o_tmem, uint64_t a0, uint64_t b0, bool accumulate) {
+    using C = TileMma<D, FP8>;
+    constexpr int VB = (C::MMA_K * 128) >> 4;
+#pragma unroll
+    for (int g = 0; g < C::PV_STEPS / 4; ++g) {
+        const uint64_t po = (uint64_t)((g * C::PANEL_BYTES) >> 4);
+        mma4_ss<2, 4, 6, VB, 2 * VB, 3 * VB, FP8>(o_tmem, a0 + po, b0 + (uint64_t)(4 * g * VB), C::ID_PV,
+                                                 (accumulate || g > 0) ? 1u : 0u);
+    }
 }
 
 }  // namespace attn

@@ -45,6 +45,19 @@ def test_fp8_small(B, H, Nq, Nk, causal):
     compare("fp8_%dx%dx%dx%d_c%d" % (B, H, Nq, Nk, causal), o, lse, o_ref, l_ref, TOL_O_FP8, TOL_LSE)
 
 
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", [(1, 2, 300, 6200, False), (1, 1, 12300, 12300, True),
+                                              (1, 1, 1000, 13000, True)])
+def test_fp8_long_rows(B, H, Nq, Nk, causal):
+    """Long rows (the decoupled prefill kernel): ragged tails, causal, Nq < Nk."""
+    q, k, v = inputs.dense_qkv(B, H, Nq, Nk, 128, seed=Nq + Nk + 1)
+    (q8, dq), (k8, dk), (v8, dv) = _quant(q, k, v)
+    scale = default_scale(128)
+    o, lse = _run(q8, k8, v8, (dq, dk, dv), causal, scale)
+    q64, k64, v64 = (x.to(torch.float64) * s for x, s in ((q8, dq), (k8, dk), (v8, dv)))
+    o_ref, l_ref = oracle.attention(q64.numpy(), k64.numpy(), v64.numpy(), scale, causal=causal)
+    compare("fp8_long_%dx%dx%dx%d_c%d" % (B, H, Nq, Nk, causal), o, lse, o_ref, l_ref, TOL_O_FP8, TOL_LSE)
+
+
 def test_fp8_workload_full():
     """B=2, H=16, N=8192, d=128: every output element against the oracle on the
     dequantised inputs.  The inputs are dequantised here, exactly, to float64
