@@ -584,8 +584,8 @@ def run_ours(args, rank, world, local_rank):
     # ---- dominant kernel roofline: the prefill kernel, one launch per step
     launch_ms = statistics.mean(step_ms)
     achieved = STEP_FLOPS / (launch_ms * 1e-3) / 1e12
-    roof = tensor_roofline(achieved, peaks, "prefill_kernel<128,bf16>",
-                           traffic_record("prefill.cu", "prefill_bf16_d128_long_causal"))
+    roof = tensor_roofline(achieved, peaks, "prefill_sp_kernel<128,bf16>",
+                           traffic_record("prefill_sp.cu", "prefill_sp_bf16_d128_long_causal"))
     roof["algorithmic_bytes"] = 3 * q.numel() * 2 + o.numel() * 2 + l.numel() * 4
     roof.update(spec.record(achieved))
 
@@ -674,9 +674,9 @@ def run_secondary(torch, attn, inputs, dev, flush, peaks, spec, rank, with_oracl
     ms = timed_launches(torch, lambda: attn.fwd_fp8(*g8, (dq, dk, dv), out=o, lse=l), reps, flush)
     attn.device_status()
     prefill_entry("fp8_prefill_2x16x8192_d128", ms, prefill_flops(2, 16, 8192, 8192, 128, False),
-                  "prefill_kernel<128,e4m3>", "prefill_fp8_d128", 
+                  "prefill_sp_kernel<128,e4m3>", "prefill_fp8_d128",
                   lambda: oracle_dense((q8, k8, v8), False, osec, descales=(dq, dk, dv), label="FP8 prefill"),
-                  fp8=True)
+                  fp8=True, kernel_file="prefill_sp.cu")
     del g8, o, l, q8, k8, v8
 
     # ---- paged decode (multi-head, CUDA cores) and grouped-query decode (tensor cores)
