@@ -52,6 +52,7 @@ namespace {
 
 constexpr float kTau = 8.0f;  // log2 units; 2^8 = 256 < 448 (e4m3 max)
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kHeadGroup = 4;  // causal unit order: heads streamed together (see unit_geometry)
 
 template <int D, bool FP8>
 struct Cfg {
@@ -135,9 +136,26 @@ __device__ __forceinline__ int tile_blocks(int q0, int rows, int Nq, int Nk, int
 __device__ __forceinline__ Unit unit_geometry(const PrefillParams& p, int u) {
     Unit g;
     int pair;
-    if (p.causal) {  // heaviest (last) pairs first, all heads of a pair adjacent
-        pair = p.n_pairs - 1 - u / p.BH;
-        g.bh = u % p.BH;
+    if (p.causal) {
+        // Heads in groups of kHeadGroup; within a group the heaviest (last)
+        // pairs first, the group's heads of a pair adjacent.  Concurrent units
+        // then stream the K/V of a few heads only, which stays in L2 (measured
+        // on 1 x 32 x 32768: DRAM reads 8.6 -> 2.2 GB per launch, and at the
+        // power cap the same time for fewer cycles' worth of clock).
+        const int hg = p.BH < kHeadGroup ? p.BH : kHeadGroup;
+        const int full = p.BH / hg, per = hg * p.n_pairs;
+        int gi, r, heads;
+        if (u < full * per) {
+            gi = u / per;
+            r = u - gi * per;
+            heads = hg;
+        } else {  // the last, smaller group
+            gi = full;
+            r = u - full * per;
+            heads = p.BH - full * hg;
+        }
+        pair = p.n_pairs - 1 - r / heads;
+        g.bh = gi * hg + r % heads;
     } else {  // all pairs of one head adjacent: concurrent units share K/V in L2
         pair = u % p.n_pairs;
         g.bh = u / p.n_pairs;

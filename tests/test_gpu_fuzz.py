@@ -46,6 +46,21 @@ def _draw(kind, n, seed):
 
 
 DENSE = _draw("dense", 24, 2024)
+
+
+def _draw_long(n, seed):
+    """Shapes whose units average 48+ key blocks: the decoupled prefill kernel."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        causal = bool(rng.integers(0, 2))
+        Nk = int(rng.integers(6200, 9000)) if not causal else int(rng.integers(12400, 16000))
+        Nq = int(rng.integers(1, 900)) if rng.integers(0, 2) else Nk - int(rng.integers(0, 300))
+        out.append(dict(B=1, H=int(rng.integers(1, 3)), Nq=Nq, Nk=Nk, d=int(rng.choice([64, 128])), causal=causal))
+    return out
+
+
+LONG = _draw_long(6, 77)
 CHUNKS = _draw("chunks", 24, 7)
 VARLEN = _draw("varlen", 16, 99)
 FP8 = [dict(c, d=128) for c in _draw("dense", 8, 5)]
@@ -75,6 +90,17 @@ def test_fuzz_dense(i):
     attn.device_status()
     o_ref, l_ref = oracle.attention(q, k, v, scale, causal=c["causal"])
     compare("fuzz_dense_%d_%s" % (i, c), o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+@pytest.mark.parametrize("i", range(len(LONG)))
+def test_fuzz_dense_long_rows(i):
+    c = LONG[i]
+    q, k, v = inputs.dense_qkv(c["B"], c["H"], c["Nq"], c["Nk"], c["d"], seed=1500 + i)
+    scale = default_scale(c["d"])
+    o, lse = attn.fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=c["causal"], scale=scale)
+    attn.device_status()
+    o_ref, l_ref = oracle.attention(q, k, v, scale, causal=c["causal"])
+    compare("fuzz_dense_long_%d_%s" % (i, c), o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
 
 
 @pytest.mark.parametrize("i", range(len(CHUNKS)))

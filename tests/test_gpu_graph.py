@@ -48,6 +48,19 @@ def test_prefill_replays_bit_identically():
     assert torch.equal(o, o_ref2) and torch.equal(l, l_ref2)
 
 
+def test_long_row_prefill_replays_bit_identically():
+    """The decoupled prefill kernel (long rows) under graph capture."""
+    q, k, v = (t.to(DEV) for t in inputs.dense_qkv(1, 2, 300, 6400, 128, seed=24))
+    o, l = torch.empty_like(q), torch.empty((1, 2, 300), dtype=torch.float32, device=DEV)
+    g = _capture(lambda: attn.fwd(q, k, v, causal=True, out=o, lse=l))
+    o_ref, l_ref = attn.fwd(q, k, v, causal=True)
+    o.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    attn.device_status()
+    assert torch.equal(o, o_ref) and torch.equal(l, l_ref)
+
+
 def test_paged_decode_and_chunks_replay_bit_identically():
     p = inputs.paged_kv(B=16, H=32, d=128, page_size=64, max_pages=32, num_pages=600, len_lo=100, len_hi=2048,
                         seed=23, device=DEV, H_kv=8)

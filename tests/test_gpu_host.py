@@ -44,6 +44,7 @@ def _device_ref(q, k, v, causal, scale):
     (1, 8, 257, 640, 64, 0),      # default chunk
     (2, 2, 130, 77, 128, 100),    # chunk larger than B*H: one chunk
     (3, 5, 513, 513, 128, 4),
+    (1, 3, 200, 6300, 128, 1),    # long rows: the decoupled prefill kernel, one head per chunk
 ])
 def test_bit_identical_to_device_path(B, H, Nq, Nk, d, chunk):
     q, k, v = (_pinned(t) for t in inputs.dense_qkv(B, H, Nq, Nk, d, seed=B * 100 + H + Nq + chunk))
