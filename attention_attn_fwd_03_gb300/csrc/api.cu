@@ -275,6 +275,7 @@ attn_status_t ragged_prefill(DeviceState* ds, const void* q, const void* k, cons
     sp.max_q_len = max_q_len;
     sp.kv_cap = kv_cap;
     sp.causal = causal;
+    sp.kv_bytes_per_key = H_kv * d * 4;
     const long long upper = (long long)B * ((max_q_len + 255) / 256) * H;  // units the list can hold
     const int grid = upper < ds->sm_count ? (int)upper : ds->sm_count;     // persistent: one CTA per SM
     return from_cuda(launch_ragged_prefill(d, sp, p, grid, stream));

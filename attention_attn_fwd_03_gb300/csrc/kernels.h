@@ -60,6 +60,7 @@ struct RaggedSched {
     int* n_listed;            // out
     unsigned* status;
     int B, H, total_q, max_q_len, kv_cap, causal;  // kv_cap: largest valid key count (paged) or key rows
+    int kv_bytes_per_key;     // K and V bytes of one key position (H_kv * d * 2 * 2)
 };
 // bytes of workspace the ragged path needs for these sizes (unit list + count)
 size_t ragged_workspace_bytes(int B, int max_q_len, int H);
