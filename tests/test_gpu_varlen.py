@@ -4,7 +4,8 @@ Packed self-attention batches (causal and not), prefixes longer than the new
 tokens, grouped KV heads from G = 1 to 8, d = 64 and 128, empty requests,
 requests with more queries than keys, one-token queries over long keys, and
 key ranges split over several CTAs and merged; the benchmark's workload in its
-launch configuration on sampled rows.  Launches whose longest
+launch configuration on sampled rows; more sequence groups than the schedule
+keeps apart, and more sequences than it groups.  Launches whose longest
 request has 128 queries or more run on the prefill kernel's ragged mode
 (query tails of any length inside a tile pair); shorter ones on the paged
 kernel, and both are covered.
@@ -104,3 +105,23 @@ def test_varlen_workload_sampled():
         hh, tt = torch.from_numpy(rows // q_len), torch.from_numpy(rows % q_len)
         compare("varlen_workload_s%d" % r, o.cpu()[q_start + tt, hh], lse.cpu()[q_start + tt, hh], o_ref, l_ref,
                 TOL_O_BF16, TOL_LSE)
+
+
+def test_varlen_many_key_groups():
+    """The schedule lists sequences in groups of about 32 MB of keys and values (longest first) and puts
+    every sequence past the 16th group into the last one: 20 sequences of ~10k keys (~40 MB each, one KV
+    head per query head) form more than 16 groups."""
+    p = inputs.varlen_qkv(B=20, H=8, H_kv=8, d=128, q_lo=128, q_hi=200, ctx_lo=9000, ctx_hi=11000, seed=47)
+    scale = default_scale(128)
+    o, lse = _run(p, scale, True)
+    o_ref, l_ref = _ref(p, scale, True)
+    compare("varlen_many_groups", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+def test_varlen_many_sequences_ungrouped():
+    """More than 4096 sequences: the schedule keeps a single longest-first list (no sequence groups)."""
+    p = inputs.varlen_qkv(B=4100, H=2, H_kv=1, d=64, q_lo=128, q_hi=128, seed=53)
+    scale = default_scale(64)
+    o, lse = _run(p, scale, True)
+    o_ref, l_ref = _ref(p, scale, True)
+    compare("varlen_4100_sequences", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
