@@ -21,13 +21,17 @@
 //               has written it (p_full[t]).  The two issuers are independent
 //               instruction streams into the tensor pipe.
 //   warps 3-6   softmax for tile 0, warps 7-10 for tile 1: one thread per
-//               row reads S from tensor memory and hands S_t back to the S
-//               issuer at once, masks, updates (m, l), forms P (bf16 or
-//               e4m3) in registers, waits until PV_t(j-1) has read P_t
-//               (pv_done[t]), writes P_t(j) as a 128-byte-swizzled K-major
-//               tile to shared memory, rescales O_t if the running max rose
-//               by more than kTau, and runs the epilogue (O / l -> bf16 rows
-//               stored directly; LSE).
+//               row reads S from tensor memory, masks, updates (m, l), forms
+//               P (bf16 or e4m3) in registers, waits until PV_t(j-1) has read
+//               P_t (pv_done[t]), writes P_t(j) as a 128-byte-swizzled
+//               K-major tile to shared memory, rescales O_t if the running max
+//               rose by more than kTau, and runs the epilogue (O / l -> bf16
+//               rows stored directly; LSE).  S_t goes back to the S issuer
+//               right after it is read -- except for bf16 rows that have seen
+//               a key: those skip the block's row max and exponentiate against
+//               the running max, and S_t is held until the block's sum shows
+//               no exponential above 2^64 (else the block is redone from S_t
+//               with its exact max).
 //
 // In prefill.cu P overwrites S in tensor memory, so S_t(j+1) can only be
 // computed after PV_t(j): the per-block chain S -> softmax -> PV -> S sets
@@ -408,19 +412,31 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
             if (!ok) break;
             tc_fence_after();
             uint32_t s[128];
-            tmem_ld32(tS + 0, s);
-            tmem_ld32(tS + 32, s + 32);
-            tmem_ld32(tS + 64, s + 64);
-            tmem_ld32(tS + 96, s + 96);
-            tmem_ld_wait();
-            reg_after_wait<128>(s);
-            tc_fence_before();
-            bar_arrive(&b.s_free[t]);  // S_t may be overwritten by S_t(it + 1) now
+            auto load_s = [&]() {
+                tmem_ld32(tS + 0, s);
+                tmem_ld32(tS + 32, s + 32);
+                tmem_ld32(tS + 64, s + 64);
+                tmem_ld32(tS + 96, s + 96);
+                tmem_ld_wait();
+                reg_after_wait<128>(s);
+            };
+            load_s();
+            // bf16 rows that have seen a key keep their running max without
+            // taking the block's row max: P may exceed 1 by far (bf16 and the
+            // fp32 sums have 8-bit exponents).  S stays in tensor memory until
+            // the block's sum shows no exponential above 2^64; otherwise the
+            // block is redone with its exact max.  (e4m3 P saturates at 448:
+            // FP8 always takes the max.)
+            const bool spec = !FP8 && __all_sync(0xffffffffu, m != -INFINITY);
+            if (!spec) {
+                tc_fence_before();
+                bar_arrive(&b.s_free[t]);  // S_t may be overwritten by S_t(it + 1) now
+            }
 
             const int kbase = it * 128;
             const bool need_mask =
                 (kbase + 128 > Nk_u) || (p.causal && (long long)kbase + 127 > (long long)q0 + off);
-            if (need_mask) {
+            auto apply_mask = [&]() {
                 // visible columns of this row: [0, bound), the keys up to
                 // min(Nk - 1, limit) (causal) or Nk - 1
                 long long last = (long long)Nk_u - 1;
@@ -430,68 +446,90 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
 #pragma unroll
                 for (int c = 0; c < 128; ++c)
                     if (c >= bound) s[c] = __float_as_uint(-INFINITY);
-            }
-            // row max: eight independent chains of 3-input max
-            float mc[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float x = __uint_as_float(s[16 * q]);
-#pragma unroll
-                for (int i = 1; i < 15; i += 2)
-                    x = max3(x, __uint_as_float(s[16 * q + i]), __uint_as_float(s[16 * q + i + 1]));
-                mc[q] = fmaxf(x, __uint_as_float(s[16 * q + 15]));
-            }
-            const float mx = fmaxf(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], max3(mc[5], mc[6], mc[7])));
-            const float m_cand = mx * cs;
+            };
             float alpha = 1.f;
             bool resc = false;
-            if (m_cand > m + kTau) {
-                if (m != -INFINITY) {
-                    alpha = ex2(m - m_cand);
-                    resc = true;
+            auto take_max = [&]() {
+                // row max: eight independent chains of 3-input max
+                float mc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    float x = __uint_as_float(s[16 * q]);
+#pragma unroll
+                    for (int i = 1; i < 15; i += 2)
+                        x = max3(x, __uint_as_float(s[16 * q + i]), __uint_as_float(s[16 * q + i + 1]));
+                    mc[q] = fmaxf(x, __uint_as_float(s[16 * q + 15]));
                 }
-                l *= alpha;
-                m = m_cand;
-            }
-            const float m_use = (m == -INFINITY) ? 0.f : m;
+                const float mx = fmaxf(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], max3(mc[5], mc[6], mc[7])));
+                const float m_cand = mx * cs;
+                if (m_cand > m + kTau) {
+                    if (m != -INFINITY) {
+                        alpha = ex2(m - m_cand);
+                        resc = true;
+                    }
+                    l *= alpha;
+                    m = m_cand;
+                }
+            };
+            if (need_mask) apply_mask();
+            if (!spec) take_max();
             // p = 2^(s * cs - m): packed FMA for the argument, MUFU ex2, packed
             // row sums; P packed (bf16 pairs / e4m3 quadruples) into registers
-            const uint64_t cs2 = f2_pack(cs, cs);
-            const uint64_t nm2 = f2_pack(-m_use, -m_use);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t w[NW];
-            if (FP8) {
+            float lsum;
+            auto exps = [&]() {
+                const float m_use = (m == -INFINITY) ? 0.f : m;
+                const uint64_t cs2 = f2_pack(cs, cs);
+                const uint64_t nm2 = f2_pack(-m_use, -m_use);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                if (FP8) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    float p0, p1, p2, p3;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1])), cs2, nm2),
-                              p0, p1);
-                    f2_unpack(
-                        f2_fma(f2_pack(__uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3])), cs2, nm2),
-                        p2, p3);
-                    p0 = ex2(p0);
-                    p1 = ex2(p1);
-                    p2 = ex2(p2);
-                    p3 = ex2(p3);
-                    acc[i & 3] = f2_add(acc[i & 3], f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
-                    w[i] = pack_e4m3x4(p0, p1, p2, p3);
-                }
-            } else {
+                    for (int i = 0; i < 32; ++i) {
+                        float p0, p1, p2, p3;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[4 * i]), __uint_as_float(s[4 * i + 1])), cs2, nm2),
+                                  p0, p1);
+                        f2_unpack(
+                            f2_fma(f2_pack(__uint_as_float(s[4 * i + 2]), __uint_as_float(s[4 * i + 3])), cs2, nm2),
+                            p2, p3);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
+                        p2 = ex2(p2);
+                        p3 = ex2(p3);
+                        acc[i & 3] = f2_add(acc[i & 3], f2_add(f2_pack(p0, p1), f2_pack(p2, p3)));
+                        w[i] = pack_e4m3x4(p0, p1, p2, p3);
+                    }
+                } else {  // exponentials over the scores in place; packed once the block is accepted
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    float p0, p1;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), cs2, nm2),
-                              p0, p1);
-                    p0 = ex2(p0);
-                    p1 = ex2(p1);
-                    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
-                    w[i] = pack_bf16(p0, p1);
+                    for (int i = 0; i < 64; ++i) {
+                        float p0, p1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), cs2, nm2),
+                                  p0, p1);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
+                        acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+                        s[2 * i] = __float_as_uint(p0);
+                        s[2 * i + 1] = __float_as_uint(p1);
+                    }
                 }
-            }
-            {
                 float a0, a1;
                 f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), a0, a1);
-                l += a0 + a1;
+                lsum = a0 + a1;
+            };
+            exps();
+            if (spec) {
+                if (__any_sync(0xffffffffu, !(lsum <= 0x1p64f))) {  // an exponential above 2^64 (or inf): redo
+                    load_s();
+                    if (need_mask) apply_mask();
+                    take_max();
+                    exps();
+                }
+                tc_fence_before();
+                bar_arrive(&b.s_free[t]);  // S_t may be overwritten by S_t(it + 1) now
+            }
+            l += lsum;
+            if (!FP8) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i) w[i] = pack_bf16(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1]));
             }
             // PV_t(it - 1) has read P_t and O_t holds it complete (the unit's
             // first block: the epilogue of the previous unit waited for its last
