@@ -27,11 +27,11 @@
 //               K-major tile to shared memory, rescales O_t if the running max
 //               rose by more than kTau, and runs the epilogue (O / l -> bf16
 //               rows stored directly; LSE).  S_t goes back to the S issuer
-//               right after it is read -- except for bf16 rows that have seen
-//               a key: those skip the block's row max and exponentiate against
+//               right after it is read -- except for rows that have seen a
+//               key: those skip the block's row max and exponentiate against
 //               the running max, and S_t is held until the block's sum shows
-//               no exponential above 2^64 (else the block is redone from S_t
-//               with its exact max).
+//               no exponential above 2^64 (bf16) or 2^kTau (e4m3), else the
+//               block is redone from S_t with its exact max.
 //
 // In prefill.cu P overwrites S in tensor memory, so S_t(j+1) can only be
 // computed after PV_t(j): the per-block chain S -> softmax -> PV -> S sets
@@ -421,13 +421,15 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
                 reg_after_wait<128>(s);
             };
             load_s();
-            // bf16 rows that have seen a key keep their running max without
-            // taking the block's row max: P may exceed 1 by far (bf16 and the
-            // fp32 sums have 8-bit exponents).  S stays in tensor memory until
-            // the block's sum shows no exponential above 2^64; otherwise the
-            // block is redone with its exact max.  (e4m3 P saturates at 448:
-            // FP8 always takes the max.)
-            const bool spec = !FP8 && __all_sync(0xffffffffu, m != -INFINITY);
+            // Rows that have seen a key keep their running max without taking
+            // the block's row max.  bf16: P may exceed 1 by far (bf16 and the
+            // fp32 sums have 8-bit exponents), so the block stands unless its
+            // sum shows an exponential above 2^64.  e4m3 (largest finite 448):
+            // it stands if the sum is at most 2^kTau -- then no p exceeds
+            // 2^kTau, exactly the case in which the kTau rule would have kept
+            // the max, so the result is the same.  S stays in tensor memory
+            // until the block stands; otherwise it is redone with its exact max.
+            const bool spec = __all_sync(0xffffffffu, m != -INFINITY);
             if (!spec) {
                 tc_fence_before();
                 bar_arrive(&b.s_free[t]);  // S_t may be overwritten by S_t(it + 1) now
@@ -517,7 +519,8 @@ __device__ void softmax_role(const PrefillParams& p, uint8_t* smem, const Bars& 
             };
             exps();
             if (spec) {
-                if (__any_sync(0xffffffffu, !(lsum <= 0x1p64f))) {  // an exponential above 2^64 (or inf): redo
+                // bf16: no exponential above 2^64; e4m3: none above 2^kTau = 256 (below its 448)
+                if (__any_sync(0xffffffffu, !(lsum <= (FP8 ? 256.f : 0x1p64f)))) {
                     load_s();
                     if (need_mask) apply_mask();
                     take_max();
