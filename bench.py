@@ -917,6 +917,10 @@ def run_profile_case(args):
         p = inputs.paged_kv(B=8, H=32, d=128, page_size=64, max_pages=128, num_pages=1024, len_lo=512,
                             len_hi=8192, seed=0, device=dev)
         fns = [lambda: attn.paged_decode(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"])]
+    elif case == "decode":  # the benchmark's paged decode workload, full size
+        p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
+                            len_hi=8192, seed=0, device=dev)
+        fns = [lambda: attn.paged_decode(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"])]
     elif case == "gqa_decode_small":
         p = inputs.paged_kv(B=16, H=32, d=128, page_size=64, max_pages=128, num_pages=2048, len_lo=512,
                             len_hi=8192, seed=0, device=dev, H_kv=8)
@@ -925,6 +929,12 @@ def run_profile_case(args):
         p = inputs.paged_kv(B=64, H=32, d=128, page_size=64, max_pages=128, num_pages=8192, len_lo=512,
                             len_hi=8192, seed=0, device=dev, H_kv=8)
         fns = [lambda: attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], p["seq_lens"])]
+    elif case == "bwd":  # the benchmark's backward workload (4 x 16 x 2048), non-causal then causal
+        q, k, v = (t.to(dev) for t in inputs.dense_qkv(B2, H2, N2, N2, D, seed=0))
+        do = torch.randn((B2, H2, N2, D), generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).to(dev)
+        fw = [attn.fwd(q, k, v, causal=c) for c in (False, True)]
+        fns = [lambda: attn.bwd(q, k, v, fw[0][0], fw[0][1], do, causal=False),
+               lambda: attn.bwd(q, k, v, fw[1][0], fw[1][1], do, causal=True)]
     elif case == "bwd_small":
         q, k, v = (t.to(dev) for t in inputs.dense_qkv(1, 8, 2048, 2048, 128, seed=0))
         do = torch.randn((1, 8, 2048, 128), generator=torch.Generator().manual_seed(1)).to(torch.bfloat16).to(dev)
@@ -971,8 +981,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", choices=["step", "batched", "long_small", "fp8", "decode_small", "gqa_decode_small",
-                                               "gqa_decode", "chunks_small", "chunks", "bwd_small", "varlen"], default=None,
+    ap.add_argument("--profile-case", choices=["step", "batched", "long_small", "fp8", "decode_small", "decode", "gqa_decode_small",
+                                               "gqa_decode", "chunks_small", "chunks", "bwd_small", "bwd", "varlen"], default=None,
                     help="run one small workload for an ncu capture instead of the benchmark")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
