@@ -77,13 +77,15 @@ attn_status_t device_state(DeviceState** out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 3-D map over a [BH, rows, d] tensor.  Operand maps: box = (128 bytes of d,
-// 128 rows, 1) with 128-byte swizzle; output map: box = (32 elements, 32
-// rows, 1), no swizzle.  Zero fill outside the tensor; stores are clipped.
-bool make_map(CUtensorMap* map, const void* base, bool fp8, int d, long long rows, long long bh, bool out) {
+// box_rows rows (128 unless given), 1) with 128-byte swizzle; output map:
+// box = (32 elements, 32 rows, 1), no swizzle.  Zero fill outside the tensor;
+// stores are clipped.
+bool make_map(CUtensorMap* map, const void* base, bool fp8, int d, long long rows, long long bh, bool out,
+              int box_rows = 128) {
     const int eb = fp8 ? 1 : 2;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)bh};
     cuuint64_t strides[2] = {(cuuint64_t)d * eb, (cuuint64_t)rows * d * eb};
-    cuuint32_t box[3] = {out ? 32u : (cuuint32_t)(128 / eb), out ? 32u : 128u, 1u};
+    cuuint32_t box[3] = {out ? 32u : (cuuint32_t)(128 / eb), out ? 32u : (cuuint32_t)box_rows, 1u};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = g_encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -657,8 +659,9 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 
     BwdParams p;
     std::memset(&p, 0, sizeof p);
-    if (!make_map(&p.tm_q, q, false, d, Nq, BH, false) || !make_map(&p.tm_k, k, false, d, Nk, BH, false) ||
-        !make_map(&p.tm_v, v, false, d, Nk, BH, false) || !make_map(&p.tm_do, dout, false, d, Nq, BH, false))
+    const int qrows = bwd_q_rows(d);  // query block height of the backward kernel
+    if (!make_map(&p.tm_q, q, false, d, Nq, BH, false, qrows) || !make_map(&p.tm_k, k, false, d, Nk, BH, false) ||
+        !make_map(&p.tm_v, v, false, d, Nk, BH, false) || !make_map(&p.tm_do, dout, false, d, Nq, BH, false, qrows))
         return ATTN_ERR_CUDA;
     const int nq_pad = (Nq + 127) / 128 * 128;
     char* ws = static_cast<char*>(workspace);

@@ -172,6 +172,10 @@ struct BwdParams {
 };
 
 constexpr int kBwdThreads = 320;  // TMA warp, MMA warp, dS warpgroup, dQ warpgroup
+// Query rows per block of the backward kernel: the height of the TMA boxes of
+// its Q and dO maps (d = 128: 64-row blocks, so two blocks' scores fit in
+// tensor memory; d = 64: 128).
+constexpr int bwd_q_rows(int d) { return d == 128 ? 64 : 128; }
 
 size_t bwd_workspace_bytes(int BH, int Nq, int d);
 cudaError_t launch_bwd(int d, const BwdParams& p, cudaStream_t stream);

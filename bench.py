@@ -840,7 +840,7 @@ def run_secondary(torch, attn, inputs, dev, flush, peaks, spec, rank, with_oracl
                              "float64 gradient oracle on 2 of the 64 (b, h) problems; FLOPs = 2.5x the forward "
                              "count (five products of the forward's size), halved for causal")
         prefill_entry("backward_4x16x2048_d128_%s" % ("causal" if causal else "non_causal"), ms,
-                      2.5 * prefill_flops(B2, H2, N2, N2, D, causal), "bwd_main_kernel<128>",
+                      2.5 * prefill_flops(B2, H2, N2, N2, D, causal), "bwd_pipe_kernel",
                       "backward_%s" % ("causal" if causal else "noncausal"), bwd_oracle, kernel_file="backward.cu")
     del q, k, v, do, ws, grads, o, l
     torch.cuda.empty_cache()

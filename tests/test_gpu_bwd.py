@@ -2,7 +2,7 @@
 
 The forward kernel supplies O and the LSE; the upstream gradient dO is a
 seeded N(0,1) bf16 tensor.  Cases: d = 64 and 128, causal and not, ragged
-lengths (tail blocks on both axes), Nq != Nk under the bottom-right causal
+lengths (tail blocks on both axes, for d = 128 also of its 64-query blocks), Nq != Nk under the bottom-right causal
 mask (rows with no visible key, keys no query sees), several heads, and the
 batched 4 x 16 x 2048 workload checked on a subset of heads.
 """
@@ -54,6 +54,9 @@ def _check(B, H, Nq, Nk, d, causal, seed, heads=None):
     (2, 3, 300, 300, 128),   # tail blocks
     (1, 2, 200, 456, 128),   # more keys than queries
     (1, 2, 456, 200, 64),    # more queries than keys: rows with no key under the causal mask
+    (1, 2, 456, 200, 128),
+    (1, 3, 40, 300, 128),    # fewer queries than one 64-row block (d = 128 runs 64-query blocks)
+    (1, 2, 65, 129, 128),    # one query past a 64-row block, one key past a 128-key block
     (2, 4, 1024, 1024, 128),
 ])
 def test_bwd(B, H, Nq, Nk, d, causal):

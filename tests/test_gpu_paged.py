@@ -103,11 +103,33 @@ def test_prefill_chunks(B, H, H_kv, d, page, max_pages, q_lo, q_hi, ctx_lo, ctx_
             o_ref, l_ref, TOL_O_BF16, TOL_LSE)
 
 
-def test_prefill_chunk_longer_than_its_keys():
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,H,H_kv,d,page,max_pages,q_lo,q_hi,ctx_lo,ctx_hi", [
+    (3, 8, 2, 128, 64, 100, 1, 300, 4000, 6000),    # long prefixes
+    (4, 8, 2, 64, 16, 400, 0, 260, 0, 6000),        # d = 64; short, long and empty requests
+    (3, 4, 4, 128, 8, 800, 128, 400, 5000, 6000),   # 8-token pages: 16 boxes per key block
+    (3, 16, 2, 128, 256, 25, 1, 200, 0, 6000),      # pages longer than a key block
+    (6, 4, 1, 128, 128, 48, 1, 130, 0, 120),        # short requests only: one key block per unit
+])
+def test_prefill_chunks_long_key_capacity(B, H, H_kv, d, page, max_pages, q_lo, q_hi, ctx_lo, ctx_hi, causal):
+    """Block tables of 6144 keys or more: long prefixes beside short and empty requests and units of
+    one key block, with the NaN-filled rest of every partial page past a sequence's end."""
+    p = inputs.paged_chunks(B=B, H=H, H_kv=H_kv, d=d, page_size=page, max_pages=max_pages,
+                            num_pages=B * max_pages + 5, q_lo=q_lo, q_hi=q_hi, ctx_lo=ctx_lo, ctx_hi=ctx_hi,
+                            seed=B * 11 + H + page)
+    scale = default_scale(d)
+    o, lse = _run(_gpu(p), scale, causal=causal, chunks=True)
+    o_ref, l_ref = _ref(p, scale, causal=causal, chunks=True)
+    compare("chunks_long_%dx%d/%d_d%d_p%d_%s" % (B, H, H_kv, d, page, "causal" if causal else "full"), o, lse,
+            o_ref, l_ref, TOL_O_BF16, TOL_LSE)
+
+
+@pytest.mark.parametrize("max_pages", [8, 100])
+def test_prefill_chunk_longer_than_its_keys(max_pages):
     """seq_len < q_len: under the causal mask the first q_len - seq_len
     queries see no key (O = 0, LSE = -inf); the rest see a prefix."""
-    p = inputs.paged_chunks(B=3, H=4, H_kv=2, d=128, page_size=64, max_pages=8, num_pages=40, q_lo=200,
-                            q_hi=260, ctx_lo=0, ctx_hi=100, seed=31)
+    p = inputs.paged_chunks(B=3, H=4, H_kv=2, d=128, page_size=64, max_pages=max_pages, num_pages=3 * max_pages + 16,
+                            q_lo=200, q_hi=260, ctx_lo=0, ctx_hi=100, seed=31)
     p["seq_lens"] = (p["seq_lens"] - torch.tensor([150, 0, 230], dtype=torch.int32)).clamp(min=0)
     scale = default_scale(128)
     o, lse = _run(_gpu(p), scale, causal=True, chunks=True)
@@ -116,14 +138,16 @@ def test_prefill_chunk_longer_than_its_keys():
     compare("chunks_short_keys", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
 
 
-def test_placement_invariance():
+@pytest.mark.parametrize("max_pages,q_lo,q_hi", [(12, 1, 100), (200, 130, 300)])
+def test_placement_invariance(max_pages, q_lo, q_hi):
     """Moving pages to other physical slots (and the table with them) gives bit-identical output."""
-    p = _gpu(inputs.paged_chunks(B=3, H=8, H_kv=2, d=128, page_size=32, max_pages=12, num_pages=40, q_lo=1,
-                                 q_hi=100, ctx_lo=0, ctx_hi=280, seed=23))
+    n = 3 * max_pages + 4
+    p = _gpu(inputs.paged_chunks(B=3, H=8, H_kv=2, d=128, page_size=32, max_pages=max_pages, num_pages=n, q_lo=q_lo,
+                                 q_hi=q_hi, ctx_lo=0, ctx_hi=280, seed=23))
     o1, l1 = _run(p, default_scale(128), causal=True, chunks=True)
-    perm = torch.randperm(40, generator=torch.Generator().manual_seed(4)).to(DEV)
+    perm = torch.randperm(n, generator=torch.Generator().manual_seed(4)).to(DEV)
     inv = torch.empty_like(perm)
-    inv[perm] = torch.arange(40, device=DEV)
+    inv[perm] = torch.arange(n, device=DEV)
     bt = p["block_table"]
     bt2 = torch.where(bt >= 0, inv[bt.clamp(min=0).long()].to(torch.int32), bt)
     p2 = dict(p, k_cache=p["k_cache"][perm].contiguous(), v_cache=p["v_cache"][perm].contiguous(),
@@ -155,10 +179,11 @@ def test_bad_device_data_is_reported():
     compare("gqa_after_error", o, lse, o_ref, l_ref, TOL_O_BF16, TOL_LSE)
 
 
-def test_bad_device_data_is_reported_for_long_chunks():
-    """The same device-data checks on the ragged path (chunks of 128 tokens or more)."""
-    p = _gpu(inputs.paged_chunks(B=3, H=8, H_kv=2, d=128, page_size=32, max_pages=20, num_pages=70, q_lo=130,
-                                 q_hi=200, ctx_lo=0, ctx_hi=300, seed=41))
+@pytest.mark.parametrize("max_pages", [20, 200])
+def test_bad_device_data_is_reported_for_long_chunks(max_pages):
+    """The same device-data checks on the ragged path (chunks of 128 tokens or more; both prefill kernels)."""
+    p = _gpu(inputs.paged_chunks(B=3, H=8, H_kv=2, d=128, page_size=32, max_pages=max_pages, num_pages=3 * max_pages + 10,
+                                 q_lo=130, q_hi=200, ctx_lo=0, ctx_hi=300, seed=41))
     sl = p["seq_lens"].clone()
     sl[1] = 100_000  # past max_pages * page_size: clamped, reported
     attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], p["block_table"], sl, cu_seqlens_q=p["cu_seqlens_q"],
@@ -167,7 +192,7 @@ def test_bad_device_data_is_reported_for_long_chunks():
         attn.device_status()
     assert ei.value.status == attn.ATTN_ERR_DEVICE_DATA
     bt = p["block_table"].clone()
-    bt[0, 0] = 70  # one past the pool: read as zeros, reported
+    bt[0, 0] = 3 * max_pages + 10  # one past the pool: read as zeros, reported
     attn.paged_fwd(p["q"], p["k_cache"], p["v_cache"], bt, p["seq_lens"], cu_seqlens_q=p["cu_seqlens_q"],
                    max_q_len=p["max_q_len"], causal=True)
     with pytest.raises(attn.AttnError) as ei:
