@@ -694,7 +694,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     p.nq_pad = nq_pad;
     p.c_scale = scale * 1.4426950408889634f;
     p.scale = scale;
-    return from_cuda(launch_bwd(d, p, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_bwd(d, p, ds->sm_count, static_cast<cudaStream_t>(stream)));
 }
 
 size_t attn_fwd_host_workspace_size(int B, int H, int Nq, int Nk, int d, int n_modes, int chunk_bh) {

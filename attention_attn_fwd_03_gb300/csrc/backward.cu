@@ -15,7 +15,8 @@
 //               with no visible key, so their P is 0), both padded to whole
 //               128-row blocks; zeroes the fp32 dQ accumulator.
 //   bwd_main    (d = 64; d = 128 runs bwd_pipe, described further down: the
-//               same products on 64-query blocks, pipelined across blocks)
+//               same products on 64-query blocks, pipelined across blocks,
+//               one persistent CTA per SM)
 //               one CTA per (batch*head, 128-key block j), K_j and V_j
 //               resident in shared memory, looping over the query blocks i
 //               that see any of its keys (all blocks, or from the diagonal on
@@ -533,6 +534,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_main_kernel(const __grid_c
 // dK products have read it: staged in the slot, as bwd_main does, the next
 // loads would wait for the reductions to read the staging out.
 //
+// The CTAs are persistent, one per SM, each taking (batch*head, key block)
+// units in turn; K_j and V_j are reloaded per unit (the next unit's pair is
+// prefetched into L2 a few blocks before the switch), and the dQ warpgroup
+// writes a unit's dV and dK while the next unit's first blocks run.
+//
 // Tensor memory, buffer b (the blocks i with i % 2 == b) at column 128 b:
 //   +0..63 S^T, then P^T (bf16 pairs) in +0..31, then dQ_i^T in +0..63;
 //   +64..127 dP^T, then dS^T in +64..95.   dV at 256, dK at 384.
@@ -557,7 +563,7 @@ struct PCfg {
     static constexpr int OFF_STG = OFF_DS + 2 * DS_TILE;  // dQ staging, 8 KB per warp of the dQ warpgroup
     static constexpr int OFF_LD = OFF_STG + STG;          // [2] x (-lse2[64], -D[64])
     static constexpr int OFF_BAR = OFF_LD + 2 * 128 * 4;
-    static constexpr int N_BARS = 1 + 2 * NQS + 4 * 2 + 2;
+    static constexpr int N_BARS = 2 + 2 * NQS + 4 * 2 + 4;
     static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -567,15 +573,18 @@ struct PCfg {
 };
 
 struct PBars {
-    uint64_t* kv_full;
-    uint64_t* qd_full;   // [NQS]
-    uint64_t* qd_empty;  // [NQS], the dV / dK products read the slot
-    uint64_t* s_full;    // [2], S^T and dP^T of the buffer's block computed
-    uint64_t* ds_ready;  // [2], 128 arrivals: P^T, dS^T in TMEM and dS in shared memory
-    uint64_t* dq_full;   // [2], dQ_i^T computed (and everything issued before it)
-    uint64_t* dq_empty;  // [2], 128 arrivals: dQ_i^T read out of TMEM
-    uint64_t* done;      // all products finished (dK, dV final)
-    uint64_t* ld_full;   // 128 arrivals per block: its lse2 / D staged
+    uint64_t* kv_full;    // K_j, V_j of the unit landed
+    uint64_t* kv_empty;   // every product of the unit done: K_j, V_j may be replaced
+    uint64_t* qd_full;    // [NQS]
+    uint64_t* qd_empty;   // [NQS], the dV / dK products read the slot
+    uint64_t* s_full;     // [2], S^T and dP^T of the buffer's block computed
+    uint64_t* ds_ready;   // [2], 128 arrivals: P^T, dS^T in TMEM and dS in shared memory
+    uint64_t* dq_full;    // [2], dQ_i^T computed (and everything issued before it)
+    uint64_t* dq_empty;   // [2], 128 arrivals: dQ_i^T read out of TMEM
+    uint64_t* acc_full;   // dV, dK of the unit final
+    uint64_t* acc_empty;  // 128 arrivals: dV, dK read out of TMEM
+    uint64_t* done;       // every product finished (before tensor memory is released)
+    uint64_t* ld_full;    // 128 arrivals per block: its lse2 / D staged
 };
 
 // First 64-query block that sees key block j (see first_qblock).
@@ -586,303 +595,414 @@ __device__ __forceinline__ int first_qblock64(const BwdParams& p, int j) {
     return (int)((need + PCfg::QB - 1) / PCfg::QB);
 }
 
+// A unit is one 128-key block j of one (batch, head).  Non-causal: the key
+// blocks of a head adjacent, so CTAs running at the same time share its Q and
+// dO in L2; causal: heaviest first (key block j sees the 64-query blocks from
+// first_qblock64(j) on), so the short units fill the tail.
+struct BUnit {
+    int bh, j, i0, nqb;
+};
+
+__device__ __forceinline__ BUnit bwd_unit(const BwdParams& p, int u) {
+    BUnit g;
+    if (p.causal) {
+        g.j = u / p.BH;
+        g.bh = u - g.j * p.BH;
+    } else {
+        g.bh = u / p.n_kblocks;
+        g.j = u - g.bh * p.n_kblocks;
+    }
+    g.i0 = first_qblock64(p, g.j);
+    const int n_all = (p.Nq + PCfg::QB - 1) / PCfg::QB;
+    g.nqb = n_all - g.i0 > 0 ? n_all - g.i0 : 0;
+    return g;
+}
+
+// This CTA's next unit: rounds of gridDim.x units, every other round in
+// reverse CTA order, or -1 when none is left.
+__device__ __forceinline__ int bwd_next_unit(int n_units, int& round_) {
+    const int G = (int)gridDim.x, c = (int)blockIdx.x;
+    for (;;) {
+        const long long base = (long long)round_ * G;
+        if (base >= n_units) return -1;
+        const int u = (int)base + ((round_ & 1) ? (G - 1 - c) : c);
+        ++round_;
+        if (u < n_units) return u;
+    }
+}
+
 __device__ __forceinline__ void st_shared_b32(uint32_t addr, uint32_t v) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-__device__ void pipe_producer(const BwdParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag, int bh,
-                              int j, int i0, int nqb) {
+// Start pulling a box into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+constexpr int kPrefetchAhead = 3;  // 64-query blocks before a unit's end: the next unit's K/V to L2
+
+__device__ void pipe_producer(const BwdParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag) {
     using C = PCfg;
     tma_prefetch_map(&p.tm_q);
     tma_prefetch_map(&p.tm_k);
     tma_prefetch_map(&p.tm_v);
     tma_prefetch_map(&p.tm_do);
-    bar_arrive_expect_tx(b.kv_full, 2 * C::KV_TILE);
-#pragma unroll
-    for (int pn = 0; pn < 2; ++pn) {
-        tma_load_3d(smem + C::OFF_K + pn * C::KV_PANEL, &p.tm_k, b.kv_full, pn * 64, j * 128, bh);
-        tma_load_3d(smem + C::OFF_V + pn * C::KV_PANEL, &p.tm_v, b.kv_full, pn * 64, j * 128, bh);
-    }
-    int issued = 0;
-    for (int it = 0; it < nqb; ++it) {
-        const int s = it % C::NQS;
-        if (it >= C::NQS && !wait_bar(&b.qd_empty[s], (uint32_t)((it / C::NQS - 1) & 1), abort_flag, p.status))
-            break;
-        const int i = i0 + it;
-        uint8_t* slot = smem + C::OFF_QD + s * C::SLOT;
-        bar_arrive_expect_tx(&b.qd_full[s], C::SLOT);
+    const int n_units = p.BH * p.n_kblocks;
+    int gq = 0, nu = 0, round_ = 0, peek_round = 0;
+    bool ok = true;
+    for (int u = bwd_next_unit(n_units, round_); ok && u >= 0; u = bwd_next_unit(n_units, round_)) {
+        const BUnit g = bwd_unit(p, u);
+        if (g.nqb == 0) continue;
+        // K_j and V_j replace the previous unit's once all its products are done
+        if (nu > 0 && !wait_bar(b.kv_empty, (uint32_t)((nu - 1) & 1), abort_flag, p.status)) break;
+        bar_arrive_expect_tx(b.kv_full, 2 * C::KV_TILE);
 #pragma unroll
         for (int pn = 0; pn < 2; ++pn) {
-            tma_load_3d(slot + pn * C::Q_PANEL, &p.tm_q, &b.qd_full[s], pn * 64, i * C::QB, bh);
-            tma_load_3d(slot + C::Q_TILE + pn * C::Q_PANEL, &p.tm_do, &b.qd_full[s], pn * 64, i * C::QB, bh);
+            tma_load_3d(smem + C::OFF_K + pn * C::KV_PANEL, &p.tm_k, b.kv_full, pn * 64, g.j * 128, g.bh);
+            tma_load_3d(smem + C::OFF_V + pn * C::KV_PANEL, &p.tm_v, b.kv_full, pn * 64, g.j * 128, g.bh);
         }
-        ++issued;
+        peek_round = round_;
+        const int un = bwd_next_unit(n_units, peek_round);
+        ++nu;
+        for (int it = 0; it < g.nqb; ++it, ++gq) {
+            // A few blocks before the unit ends the next unit's K and V start
+            // towards L2, so that their load at the unit boundary hits there
+            // (issued earlier, the streams of Q, dO and the dQ reductions
+            // evict them again).
+            if (un >= 0 && it == (g.nqb > kPrefetchAhead ? g.nqb - kPrefetchAhead : 0)) {
+                const BUnit gn = bwd_unit(p, un);
+#pragma unroll
+                for (int pn = 0; pn < 2; ++pn) {
+                    tma_prefetch_l2_3d(&p.tm_k, pn * 64, gn.j * 128, gn.bh);
+                    tma_prefetch_l2_3d(&p.tm_v, pn * 64, gn.j * 128, gn.bh);
+                }
+            }
+            const int s = gq % C::NQS;
+            if (gq >= C::NQS && !wait_bar(&b.qd_empty[s], (uint32_t)((gq / C::NQS - 1) & 1), abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            const int i = g.i0 + it;
+            uint8_t* slot = smem + C::OFF_QD + s * C::SLOT;
+            bar_arrive_expect_tx(&b.qd_full[s], C::SLOT);
+#pragma unroll
+            for (int pn = 0; pn < 2; ++pn) {
+                tma_load_3d(slot + pn * C::Q_PANEL, &p.tm_q, &b.qd_full[s], pn * 64, i * C::QB, g.bh);
+                tma_load_3d(slot + C::Q_TILE + pn * C::Q_PANEL, &p.tm_do, &b.qd_full[s], pn * 64, i * C::QB, g.bh);
+            }
+        }
     }
     // every copy started here lands before the CTA exits
-    drain_wait(b.kv_full, 0, p.status);
-    for (int it = issued - C::NQS > 0 ? issued - C::NQS : 0; it < issued; ++it)
-        drain_wait(&b.qd_full[it % C::NQS], (uint32_t)((it / C::NQS) & 1), p.status);
+    if (nu > 0) drain_wait(b.kv_full, (uint32_t)((nu - 1) & 1), p.status);
+    for (int q = gq - C::NQS > 0 ? gq - C::NQS : 0; q < gq; ++q)
+        drain_wait(&b.qd_full[q % C::NQS], (uint32_t)((q / C::NQS) & 1), p.status);
 }
 
-// One thread.  Step it issues S^T, dP^T of block it into buffer it % 2 (once
-// dQ_{it-2}^T has left it), then the dV, dK and dQ^T products of block it - 1
-// (once its dS is ready); a last step issues those of the final block.
-__device__ void pipe_mma(const BwdParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag, uint32_t tmem,
-                         int nqb) {
+// One thread.  Per unit, step it issues S^T, dP^T of block it into buffer
+// (global block) % 2 once dQ^T of the block two before has left it, then the
+// dV, dK and dQ^T products of block it - 1 once its dS is ready; a last step
+// issues those of the unit's final block.  Block counters run on across units.
+__device__ void pipe_mma(const BwdParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag,
+                         uint32_t tmem) {
     using C = PCfg;
     const uint32_t sb = smem_u32(smem);
     const uint64_t k_kmaj = sdesc_sw128(sb + C::OFF_K, 16, 1024);
     const uint64_t v_kmaj = sdesc_sw128(sb + C::OFF_V, 16, 1024);
     const uint64_t k_mn = sdesc_sw128(sb + C::OFF_K, C::KV_PANEL, 1024);  // K_j^T: head dims along M
     constexpr int KVP = C::KV_PANEL >> 4, QP = C::Q_PANEL >> 4;           // panel strides, descriptor units
-    if (!wait_bar(b.kv_full, 0, abort_flag, p.status)) return;
-    for (int it = 0; it <= nqb; ++it) {
-        if (it < nqb) {
-            const int s = it % C::NQS, bf = it & 1;
-            const uint32_t q_addr = sb + C::OFF_QD + s * C::SLOT, do_addr = q_addr + C::Q_TILE;
-            if (!wait_bar(&b.qd_full[s], (uint32_t)((it / C::NQS) & 1), abort_flag, p.status)) return;
-            if (it >= 2 && !wait_bar(&b.dq_empty[bf], (uint32_t)(((it - 2) >> 1) & 1), abort_flag, p.status)) return;
-            tc_fence_after();
-            const uint32_t t_s = tmem + 128u * (uint32_t)bf;
-            // S^T = K_j Q_i^T, dP^T = V_j dO_i^T: 8 steps of 16 head dims (32 bytes);
-            // K and V advance a 16 KB panel every 4 steps, Q and dO an 8 KB one
-            const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), dd = sdesc_sw128(do_addr, 16, 1024);
-            mma4_ss<2, 4, 6, 2, 4, 6, false>(t_s, k_kmaj, qd, C::ID_S, 0u);
-            mma4_ss<2, 4, 6, 2, 4, 6, false>(t_s, k_kmaj + KVP, qd + QP, C::ID_S, 1u);
-            mma4_ss<2, 4, 6, 2, 4, 6, false>(t_s + 64, v_kmaj, dd, C::ID_S, 0u);
-            mma4_ss<2, 4, 6, 2, 4, 6, false>(t_s + 64, v_kmaj + KVP, dd + QP, C::ID_S, 1u);
-            tc_commit(&b.s_full[bf]);
+    const int n_units = p.BH * p.n_kblocks;
+    int gb = 0, nu = 0, round_ = 0;
+    for (int u = bwd_next_unit(n_units, round_); u >= 0; u = bwd_next_unit(n_units, round_)) {
+        const BUnit g = bwd_unit(p, u);
+        if (g.nqb == 0) continue;
+        if (!wait_bar(b.kv_full, (uint32_t)(nu & 1), abort_flag, p.status)) return;
+        for (int it = 0; it <= g.nqb; ++it) {
+            if (it < g.nqb) {
+                const int q = gb + it, s = q % C::NQS, bf = q & 1;
+                const uint32_t q_addr = sb + C::OFF_QD + s * C::SLOT, do_addr = q_addr + C::Q_TILE;
+                if (!wait_bar(&b.qd_full[s], (uint32_t)((q / C::NQS) & 1), abort_flag, p.status)) return;
+                if (q >= 2 && !wait_bar(&b.dq_empty[bf], (uint32_t)(((q - 2) >> 1) & 1), abort_flag, p.status))
+                    return;
+                tc_fence_after();
+                const uint32_t t_s = tmem + 128u * (uint32_t)bf;
+                // S^T = K_j Q_i^T, dP^T = V_j dO_i^T: 8 steps of 16 head dims (32 bytes);
+                // K and V advance a 16 KB panel every 4 steps, Q and dO an 8 KB one
+                const uint64_t qd = sdesc_sw128(q_addr, 16, 1024), dd = sdesc_sw128(do_addr, 16, 1024);
+                mma4_ss<2, 4, 6, 2, 4, 6, false>(t_s, k_kmaj, qd, C::ID_S, 0u);
+                mma4_ss<2, 4, 6, 2, 4, 6, false>(t_s, k_kmaj + KVP, qd + QP, C::ID_S, 1u);
+                mma4_ss<2, 4, 6, 2, 4, 6, false>(t_s + 64, v_kmaj, dd, C::ID_S, 0u);
+                mma4_ss<2, 4, 6, 2, 4, 6, false>(t_s + 64, v_kmaj + KVP, dd + QP, C::ID_S, 1u);
+                tc_commit(&b.s_full[bf]);
+            }
+            if (it >= 1) {
+                const int q = gb + it - 1, s = q % C::NQS, bf = q & 1;
+                const uint32_t q_addr = sb + C::OFF_QD + s * C::SLOT, do_addr = q_addr + C::Q_TILE;
+                if (!wait_bar(&b.ds_ready[bf], (uint32_t)((q >> 1) & 1), abort_flag, p.status)) return;
+                // the unit's first dV / dK product overwrites the accumulators:
+                // the previous unit's must have been read out
+                if (it == 1 && nu > 0 &&
+                    !wait_bar(b.acc_empty, (uint32_t)((nu - 1) & 1), abort_flag, p.status))
+                    return;
+                tc_fence_after();
+                const uint32_t t_s = tmem + 128u * (uint32_t)bf;
+                // dV += P^T dO_i, dK += dS^T Q_i: 4 steps of 16 queries (8 TMEM columns of bf16
+                // pairs; the MN-major B advances 16 rows, 2 KB)
+                mma4_ts<8, 16, 24, 128, 256, 384, false>(tmem + C::TM_DV, t_s, sdesc_sw128(do_addr, C::Q_PANEL, 1024),
+                                                         C::ID_G, it > 1 ? 1u : 0u);
+                mma4_ts<8, 16, 24, 128, 256, 384, false>(tmem + C::TM_DK, t_s + 64,
+                                                         sdesc_sw128(q_addr, C::Q_PANEL, 1024), C::ID_G,
+                                                         it > 1 ? 1u : 0u);
+                tc_commit(&b.qd_empty[s]);
+                if (it == g.nqb) tc_commit(b.acc_full);
+                // dQ_i^T = K_j^T dS_i^T: 8 steps of 16 keys, both operands advance 16 rows (2 KB)
+                const uint64_t dsd = sdesc_sw128(sb + C::OFF_DS + bf * C::DS_TILE, C::DS_TILE, 1024);
+                mma4_ss<128, 256, 384, 128, 256, 384, false>(t_s, k_mn, dsd, C::ID_DQT, 0u);
+                mma4_ss<128, 256, 384, 128, 256, 384, false>(t_s, k_mn + 512, dsd + 512, C::ID_DQT, 1u);
+                tc_commit(&b.dq_full[bf]);
+            }
         }
-        if (it >= 1) {
-            const int k = it - 1, s = k % C::NQS, bf = k & 1;
-            const uint32_t q_addr = sb + C::OFF_QD + s * C::SLOT, do_addr = q_addr + C::Q_TILE;
-            if (!wait_bar(&b.ds_ready[bf], (uint32_t)((k >> 1) & 1), abort_flag, p.status)) return;
-            tc_fence_after();
-            const uint32_t t_s = tmem + 128u * (uint32_t)bf;
-            // dV += P^T dO_i, dK += dS^T Q_i: 4 steps of 16 queries (8 TMEM columns of bf16
-            // pairs; the MN-major B advances 16 rows, 2 KB)
-            mma4_ts<8, 16, 24, 128, 256, 384, false>(tmem + C::TM_DV, t_s, sdesc_sw128(do_addr, C::Q_PANEL, 1024),
-                                                     C::ID_G, k > 0 ? 1u : 0u);
-            mma4_ts<8, 16, 24, 128, 256, 384, false>(tmem + C::TM_DK, t_s + 64, sdesc_sw128(q_addr, C::Q_PANEL, 1024),
-                                                     C::ID_G, k > 0 ? 1u : 0u);
-            tc_commit(&b.qd_empty[s]);
-            // dQ_i^T = K_j^T dS_i^T: 8 steps of 16 keys, both operands advance 16 rows (2 KB)
-            const uint64_t dsd = sdesc_sw128(sb + C::OFF_DS + bf * C::DS_TILE, C::DS_TILE, 1024);
-            mma4_ss<128, 256, 384, 128, 256, 384, false>(t_s, k_mn, dsd, C::ID_DQT, 0u);
-            mma4_ss<128, 256, 384, 128, 256, 384, false>(t_s, k_mn + 512, dsd + 512, C::ID_DQT, 1u);
-            tc_commit(&b.dq_full[bf]);
-        }
+        tc_commit(b.kv_empty);  // K_j, V_j read by every product of the unit
+        gb += g.nqb;
+        ++nu;
     }
 }
 
-// One thread per key row (TMEM lane): P^T and dS^T of each 64-query block,
-// then the dK, dV epilogue.
+// One thread per key row (TMEM lane): P^T and dS^T of each 64-query block of
+// every unit.
 __device__ void pipe_ds_role(const BwdParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag,
-                             uint32_t tmem, int bh, int j, int i0, int nqb, int wq, int lane) {
+                             uint32_t tmem, int wq, int lane) {
     using C = PCfg;
-    constexpr int D = C::D;
     const int row = wq * 32 + lane;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    const int key = j * 128 + row;
-    const bool key_ok = key < p.Nk;
     const int off = p.Nk - p.Nq;
     const float cs = p.c_scale;
     float* lds = reinterpret_cast<float*>(smem + C::OFF_LD);  // [2][128]: -lse2 of the block's queries, then -D
-    // this thread's entry of each block -- lse2 (rows 0-63) or D (64-127) -- loaded a block ahead
-    const float* src = (row < C::QB ? p.lse2 + row : p.dvec + (row - C::QB)) + (size_t)bh * p.nq_pad +
-                       (size_t)i0 * C::QB;
-    float nx = nqb > 0 ? src[0] : 0.f;
+    const int n_units = p.BH * p.n_kblocks;
+    int gb = 0, round_ = 0;
     bool ok = true;
-    for (int it = 0; ok && it < nqb; ++it) {
-        const int i = i0 + it, bf = it & 1;
-        const float mine = nx;
-        if (it + 1 < nqb) nx = src[(size_t)(it + 1) * C::QB];
-        // Buffer bf held block it - 2's entries: every thread finished that
-        // block before it arrived for block it - 1, which this thread has seen.
-        lds[bf * 128 + row] = -mine;  // negated: the score step is one fma, the dS step one add
-        bar_arrive(b.ld_full);
-        ok = __all_sync(0xffffffffu, wait_bar(b.ld_full, (uint32_t)(it & 1), abort_flag, p.status));
-        if (!ok) break;
-        // S^T, dP^T ready; their commit also covers dQ_{it-2}^T, the last reader of dS buffer bf
-        ok = __all_sync(0xffffffffu, wait_bar(&b.s_full[bf], (uint32_t)((it >> 1) & 1), abort_flag, p.status));
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t tS = tmem + lane_off + 128u * (uint32_t)bf, tP = tS + 64;
-        const uint32_t ds_row = smem_u32(smem + C::OFF_DS + bf * C::DS_TILE) + (uint32_t)(row * 128);
-        // Queries of this block before `vis_from` do not see this key (causal
-        // mask); the whole warp takes the mask-free path when none of its keys
-        // needs it.  Scores, shifts and products run as packed pairs.
-        const int vis_from = key_ok ? (p.causal ? key - off - i * C::QB : 0) : C::QB;
-        const bool all_visible = __all_sync(0xffffffffu, vis_from <= 0);
-        const float* nl = lds + bf * 128;  // -lse2 of the block's queries
-        const float* nd = nl + C::QB;      // -D
-        const uint64_t cs2 = f2_pack(cs, cs);
+    for (int u = bwd_next_unit(n_units, round_); ok && u >= 0; u = bwd_next_unit(n_units, round_)) {
+        const BUnit g = bwd_unit(p, u);
+        const int key = g.j * 128 + row;
+        const bool key_ok = key < p.Nk;
+        // this thread's entry of each block -- lse2 (rows 0-63) or D (64-127) -- loaded a block ahead
+        const float* src = (row < C::QB ? p.lse2 + row : p.dvec + (row - C::QB)) + (size_t)g.bh * p.nq_pad +
+                           (size_t)g.i0 * C::QB;
+        float nx = g.nqb > 0 ? src[0] : 0.f;
+        for (int it = 0; it < g.nqb; ++it) {
+            const int q = gb + it, i = g.i0 + it, bf = q & 1;
+            const float mine = nx;
+            if (it + 1 < g.nqb) nx = src[(size_t)(it + 1) * C::QB];
+            // Buffer bf held the entries of the block two before: every thread
+            // finished that block before it arrived for the previous one, which
+            // this thread has seen.
+            lds[bf * 128 + row] = -mine;  // negated: the score step is one fma, the dS step one add
+            bar_arrive(b.ld_full);
+            ok = __all_sync(0xffffffffu, wait_bar(b.ld_full, (uint32_t)(q & 1), abort_flag, p.status));
+            if (!ok) break;
+            // S^T, dP^T ready; their commit also covers dQ^T of the block two
+            // before, the last reader of dS buffer bf
+            ok = __all_sync(0xffffffffu, wait_bar(&b.s_full[bf], (uint32_t)((q >> 1) & 1), abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tS = tmem + lane_off + 128u * (uint32_t)bf, tP = tS + 64;
+            const uint32_t ds_row = smem_u32(smem + C::OFF_DS + bf * C::DS_TILE) + (uint32_t)(row * 128);
+            // Queries of this block before `vis_from` do not see this key (causal
+            // mask); the whole warp takes the mask-free path when none of its keys
+            // needs it.  Scores, shifts and products run as packed pairs.
+            const int vis_from = key_ok ? (p.causal ? key - off - i * C::QB : 0) : C::QB;
+            const bool all_visible = __all_sync(0xffffffffu, vis_from <= 0);
+            const float* nl = lds + bf * 128;  // -lse2 of the block's queries
+            const float* nd = nl + C::QB;      // -D
+            const uint64_t cs2 = f2_pack(cs, cs);
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {  // 32 queries per chunk
-            uint32_t sv[32], dp[32];
-            tmem_ld32(tS + 32 * c, sv);
-            tmem_ld32(tP + 32 * c, dp);
-            tmem_ld_wait();
-            reg_after_wait<32>(sv);
-            reg_after_wait<32>(dp);
-            uint32_t pw[16], dw[16];
+            for (int c = 0; c < 2; ++c) {  // 32 queries per chunk
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tS + 32 * c, sv);
+                tmem_ld32(tP + 32 * c, dp);
+                tmem_ld_wait();
+                reg_after_wait<32>(sv);
+                reg_after_wait<32>(dp);
+                uint32_t pw[16], dw[16];
 #pragma unroll
-            for (int t4 = 0; t4 < 8; ++t4) {
-                const float4 L = *reinterpret_cast<const float4*>(nl + 32 * c + 4 * t4);
-                const float4 Dn = *reinterpret_cast<const float4*>(nd + 32 * c + 4 * t4);
+                for (int t4 = 0; t4 < 8; ++t4) {
+                    const float4 L = *reinterpret_cast<const float4*>(nl + 32 * c + 4 * t4);
+                    const float4 Dn = *reinterpret_cast<const float4*>(nd + 32 * c + 4 * t4);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int t = 4 * t4 + 2 * h;
-                    const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), cs2,
-                                              h ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y));
-                    float p0, p1;
-                    f2_unpack(x, p0, p1);
-                    p0 = ex2(p0);
-                    p1 = ex2(p1);
-                    if (!all_visible) {
-                        const int tq = 32 * c + t;  // query index within the block
-                        p0 = tq >= vis_from ? p0 : 0.f;
-                        p1 = tq + 1 >= vis_from ? p1 : 0.f;
+                    for (int h = 0; h < 2; ++h) {
+                        const int t = 4 * t4 + 2 * h;
+                        const uint64_t x = f2_fma(f2_pack(__uint_as_float(sv[t]), __uint_as_float(sv[t + 1])), cs2,
+                                                  h ? f2_pack(L.z, L.w) : f2_pack(L.x, L.y));
+                        float p0, p1;
+                        f2_unpack(x, p0, p1);
+                        p0 = ex2(p0);
+                        p1 = ex2(p1);
+                        if (!all_visible) {
+                            const int tq = 32 * c + t;  // query index within the block
+                            p0 = tq >= vis_from ? p0 : 0.f;
+                            p1 = tq + 1 >= vis_from ? p1 : 0.f;
+                        }
+                        const uint64_t pp = f2_pack(p0, p1);
+                        const uint64_t diff = f2_add(f2_pack(__uint_as_float(dp[t]), __uint_as_float(dp[t + 1])),
+                                                     h ? f2_pack(Dn.z, Dn.w) : f2_pack(Dn.x, Dn.y));
+                        float d0, d1;
+                        f2_unpack(f2_mul(pp, diff), d0, d1);
+                        pw[2 * t4 + h] = pack_bf16(p0, p1);
+                        dw[2 * t4 + h] = pack_bf16(d0, d1);
                     }
-                    const uint64_t pp = f2_pack(p0, p1);
-                    const uint64_t diff = f2_add(f2_pack(__uint_as_float(dp[t]), __uint_as_float(dp[t + 1])),
-                                                 h ? f2_pack(Dn.z, Dn.w) : f2_pack(Dn.x, Dn.y));
-                    float d0, d1;
-                    f2_unpack(f2_mul(pp, diff), d0, d1);
-                    pw[2 * t4 + h] = pack_bf16(p0, p1);
-                    dw[2 * t4 + h] = pack_bf16(d0, d1);
+                }
+                tmem_st16(tS + 16 * c, pw);
+                tmem_st16(tP + 16 * c, dw);
+                // dS row `row`, queries 32c..32c+31: 16-byte chunks 4c..4c+3 of the
+                // 128-byte row, 128-byte swizzle (chunk ^ row % 8)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t chunk = (uint32_t)(4 * c + k) ^ (uint32_t)(row & 7);
+                    st_shared_v4(ds_row + chunk * 16u, dw[4 * k], dw[4 * k + 1], dw[4 * k + 2], dw[4 * k + 3]);
                 }
             }
-            tmem_st16(tS + 16 * c, pw);
-            tmem_st16(tP + 16 * c, dw);
-            // dS row `row`, queries 32c..32c+31: 16-byte chunks 4c..4c+3 of the
-            // 128-byte row, 128-byte swizzle (chunk ^ row % 8)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t chunk = (uint32_t)(4 * c + k) ^ (uint32_t)(row & 7);
-                st_shared_v4(ds_row + chunk * 16u, dw[4 * k], dw[4 * k + 1], dw[4 * k + 2], dw[4 * k + 3]);
-            }
+            tmem_st_wait();
+            fence_async_smem();
+            tc_fence_before();
+            bar_arrive(&b.ds_ready[bf]);
         }
-        tmem_st_wait();
-        fence_async_smem();
-        tc_fence_before();
-        bar_arrive(&b.ds_ready[bf]);
+        gb += g.nqb;
     }
-    if (!ok) return;
-    // ---- epilogue: dV and scale * dK rows of this key block -> bf16
-    if (nqb > 0) {
-        ok = __all_sync(0xffffffffu, wait_bar(b.done, 0, abort_flag, p.status));
-        if (!ok) return;
+}
+
+// dV and scale * dK rows of one unit's key block -> bf16 (one thread per key
+// row, i.e. TMEM lane); zeros when no query sees the block.
+__device__ __forceinline__ bool pipe_epilogue(const BwdParams& p, const PBars& b, volatile int* abort_flag,
+                                              uint32_t tmem, const BUnit& g, int nu, int row, uint32_t lane_off) {
+    using C = PCfg;
+    constexpr int D = C::D;
+    const int key = g.j * 128 + row;
+    if (g.nqb > 0) {
+        if (!__all_sync(0xffffffffu, wait_bar(b.acc_full, (uint32_t)(nu & 1), abort_flag, p.status))) return false;
         tc_fence_after();
     }
-    uint16_t* dvr = p.dv + ((size_t)bh * p.Nk + key) * D;
-    uint16_t* dkr = p.dk + ((size_t)bh * p.Nk + key) * D;
+    uint16_t* dvr = p.dv + ((size_t)g.bh * p.Nk + key) * D;
+    uint16_t* dkr = p.dk + ((size_t)g.bh * p.Nk + key) * D;
+    const float sc = p.scale;
 #pragma unroll 1
     for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t a[32], g[32];
-        if (nqb > 0) {
+        uint32_t a[32], gk[32];
+        if (g.nqb > 0) {
             tmem_ld32(tmem + lane_off + C::TM_DV + 32 * ch, a);
-            tmem_ld32(tmem + lane_off + C::TM_DK + 32 * ch, g);
+            tmem_ld32(tmem + lane_off + C::TM_DK + 32 * ch, gk);
             tmem_ld_wait();
             reg_after_wait<32>(a);
-            reg_after_wait<32>(g);
-        } else {  // no query sees this block: zero gradients
+            reg_after_wait<32>(gk);
+            if (ch == D / 32 - 1) {  // the accumulators are free for the next unit
+                tc_fence_before();
+                bar_arrive(b.acc_empty);
+            }
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
+            for (int e = 0; e < 32; ++e) a[e] = gk[e] = 0u;
         }
-        if (key_ok) {
+        if (key < p.Nk) {
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
                 st_global_v4(dvr + 32 * ch + e, pack_bf16(__uint_as_float(a[e]), __uint_as_float(a[e + 1])),
                              pack_bf16(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3])),
                              pack_bf16(__uint_as_float(a[e + 4]), __uint_as_float(a[e + 5])),
                              pack_bf16(__uint_as_float(a[e + 6]), __uint_as_float(a[e + 7])));
-                const float sc = p.scale;
                 st_global_v4(dkr + 32 * ch + e,
-                             pack_bf16(__uint_as_float(g[e]) * sc, __uint_as_float(g[e + 1]) * sc),
-                             pack_bf16(__uint_as_float(g[e + 2]) * sc, __uint_as_float(g[e + 3]) * sc),
-                             pack_bf16(__uint_as_float(g[e + 4]) * sc, __uint_as_float(g[e + 5]) * sc),
-                             pack_bf16(__uint_as_float(g[e + 6]) * sc, __uint_as_float(g[e + 7]) * sc));
+                             pack_bf16(__uint_as_float(gk[e]) * sc, __uint_as_float(gk[e + 1]) * sc),
+                             pack_bf16(__uint_as_float(gk[e + 2]) * sc, __uint_as_float(gk[e + 3]) * sc),
+                             pack_bf16(__uint_as_float(gk[e + 4]) * sc, __uint_as_float(gk[e + 5]) * sc),
+                             pack_bf16(__uint_as_float(gk[e + 6]) * sc, __uint_as_float(gk[e + 7]) * sc));
             }
         }
     }
+    return true;
 }
 
-// One thread per head dim (TMEM lane of dQ_i^T): the block's 64 dQ values
-// added into the accumulator.
+// dQ warpgroup: per block one thread per head dim (TMEM lane of dQ_i^T), the
+// block's 64 dQ values added into the accumulator; after a unit's last block,
+// one thread per key row for its dV, dK epilogue.
 __device__ void pipe_dq_role(const BwdParams& p, uint8_t* smem, const PBars& b, volatile int* abort_flag,
-                             uint32_t tmem, int bh, int i0, int nqb, int wq, int lane) {
+                             uint32_t tmem, int wq, int lane) {
     using C = PCfg;
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;  // head dims 32 wq .. 32 wq + 31
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;  // head dims (dQ^T) or key rows (dV, dK) 32 wq ..
     if (lane == 0) tma_prefetch_map(&p.tm_dq);
-    for (int it = 0; it < nqb; ++it) {
-        const int bf = it & 1;
-        const bool okw =
-            __all_sync(0xffffffffu, wait_bar(&b.dq_full[bf], (uint32_t)((it >> 1) & 1), abort_flag, p.status));
-        if (!okw) break;
-        tc_fence_after();
-        uint32_t v[C::QB];  // this head dim of the block's 64 queries
-        tmem_ld32(tmem + lane_off + 128u * (uint32_t)bf, v);
-        tmem_ld32(tmem + lane_off + 128u * (uint32_t)bf + 32, v + 32);
-        tmem_ld_wait();
-        reg_after_wait<C::QB>(v);
-        tc_fence_before();
-        bar_arrive(&b.dq_empty[bf]);
-        // Stage the warp's 32 head dims x 64 queries as two boxes of 32 query
-        // rows x 32 fp32 (128-byte rows, 128-byte swizzle: 16-byte chunk k of
-        // row r at k ^ (r % 8)) once the engine has read the previous block's,
-        // then let the bulk-copy engine add them into the accumulator.
-        if (lane == 0) tma_wait_read_all();
-        __syncwarp();
-        uint8_t* stage_p = smem + C::OFF_STG + wq * 8192;
-        const uint32_t stage = smem_u32(stage_p) + (uint32_t)((lane & 3) * 4);
+    uint8_t* stage_p = smem + C::OFF_STG + wq * 8192;
+    const uint32_t stage = smem_u32(stage_p) + (uint32_t)((lane & 3) * 4);
+    const int n_units = p.BH * p.n_kblocks;
+    int gb = 0, nu = 0, round_ = 0;
+    bool ok = true;
+    for (int u = bwd_next_unit(n_units, round_); ok && u >= 0; u = bwd_next_unit(n_units, round_)) {
+        const BUnit g = bwd_unit(p, u);
+        for (int it = 0; it < g.nqb; ++it) {
+            const int q = gb + it, bf = q & 1;
+            ok = __all_sync(0xffffffffu, wait_bar(&b.dq_full[bf], (uint32_t)((q >> 1) & 1), abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[C::QB];  // this head dim of the block's 64 queries
+            tmem_ld32(tmem + lane_off + 128u * (uint32_t)bf, v);
+            tmem_ld32(tmem + lane_off + 128u * (uint32_t)bf + 32, v + 32);
+            tmem_ld_wait();
+            reg_after_wait<C::QB>(v);
+            tc_fence_before();
+            bar_arrive(&b.dq_empty[bf]);
+            // Stage the warp's 32 head dims x 64 queries as two boxes of 32 query
+            // rows x 32 fp32 (128-byte rows, 128-byte swizzle: 16-byte chunk k of
+            // row r at k ^ (r % 8)) once the engine has read the previous block's,
+            // then let the bulk-copy engine add them into the accumulator.
+            if (lane == 0) tma_wait_read_all();
+            __syncwarp();
 #pragma unroll
-        for (int q = 0; q < C::QB; ++q)
-            st_shared_b32(stage + (uint32_t)((q >> 5) * 4096 + (q & 31) * 128) +
-                              ((((uint32_t)lane >> 2) ^ (uint32_t)(q & 7)) << 4),
-                          v[q]);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            const int row0 = (i0 + it) * C::QB;
-            tma_reduce_add_3d(&p.tm_dq, stage_p, wq * 32, row0, bh);
-            tma_reduce_add_3d(&p.tm_dq, stage_p + 4096, wq * 32, row0 + 32, bh);
-            tma_store_commit();
+            for (int qq = 0; qq < C::QB; ++qq)
+                st_shared_b32(stage + (uint32_t)((qq >> 5) * 4096 + (qq & 31) * 128) +
+                                  ((((uint32_t)lane >> 2) ^ (uint32_t)(qq & 7)) << 4),
+                              v[qq]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const int row0 = (g.i0 + it) * C::QB;
+                tma_reduce_add_3d(&p.tm_dq, stage_p, wq * 32, row0, g.bh);
+                tma_reduce_add_3d(&p.tm_dq, stage_p + 4096, wq * 32, row0 + 32, g.bh);
+                tma_store_commit();
+            }
+            __syncwarp();
         }
-        __syncwarp();
+        if (!ok) break;
+        ok = pipe_epilogue(p, b, abort_flag, tmem, g, nu, wq * 32 + lane, lane_off);
+        gb += g.nqb;
+        nu += g.nqb > 0;
     }
     if (lane == 0) tma_store_wait_all();  // every reduction has landed before the CTA exits
     __syncwarp();
 }
 
+// Persistent: one CTA per SM takes (batch*head, key block) units in snake
+// order; K_j and V_j are reloaded per unit, the dV / dK epilogue of a unit
+// runs while the next unit's first blocks are computed.
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_pipe_kernel(const __grid_constant__ BwdParams p) {
     using C = PCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // CTA order as for bwd_main_kernel: non-causal head-major, causal heaviest key block first
-    int j = blockIdx.x, bh = blockIdx.y;
-    if (p.causal) {
-        const long long lin = (long long)blockIdx.y * gridDim.x + blockIdx.x;
-        j = (int)(lin / p.BH);
-        bh = (int)(lin % p.BH);
-    }
-    const int i0 = first_qblock64(p, j);
-    const int n_all = (p.Nq + C::QB - 1) / C::QB;
-    const int nqb = n_all - i0 > 0 ? n_all - i0 : 0;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     PBars b;
     b.kv_full = bars;
-    b.qd_full = bars + 1;
+    b.kv_empty = bars + 1;
+    b.qd_full = bars + 2;
     b.qd_empty = b.qd_full + C::NQS;
     b.s_full = b.qd_empty + C::NQS;
     b.ds_ready = b.s_full + 2;
     b.dq_full = b.ds_ready + 2;
     b.dq_empty = b.dq_full + 2;
-    b.done = b.dq_empty + 2;
+    b.acc_full = b.dq_empty + 2;
+    b.acc_empty = b.acc_full + 1;
+    b.done = b.acc_empty + 1;
     b.ld_full = b.done + 1;
-    static_assert(1 + 2 * PCfg::NQS + 8 + 2 == PCfg::N_BARS, "barrier count");
+    static_assert(2 + 2 * PCfg::NQS + 8 + 4 == PCfg::N_BARS, "barrier count");
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
     volatile int* skip = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
@@ -893,6 +1013,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_pipe_kernel(const __grid_c
 
     if (threadIdx.x == 0) {
         bar_init(b.kv_full, 1);
+        bar_init(b.kv_empty, 1);
         for (int s = 0; s < C::NQS; ++s) {
             bar_init(&b.qd_full[s], 1);
             bar_init(&b.qd_empty[s], 1);
@@ -903,6 +1024,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_pipe_kernel(const __grid_c
             bar_init(&b.dq_full[t], 1);
             bar_init(&b.dq_empty[t], 128);
         }
+        bar_init(b.acc_full, 1);
+        bar_init(b.acc_empty, 128);
         bar_init(b.done, 1);
         bar_init(b.ld_full, 128);
         *abort_flag = 0;
@@ -918,18 +1041,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_pipe_kernel(const __grid_c
     const uint32_t tmem = *tmem_holder;
 
     if (warp >= 2 && warp < 6) {
-        pipe_ds_role(p, smem, b, abort_flag, tmem, bh, j, i0, nqb, warp & 3, lane);
+        pipe_ds_role(p, smem, b, abort_flag, tmem, warp & 3, lane);
     } else if (warp >= 6) {
-        pipe_dq_role(p, smem, b, abort_flag, tmem, bh, i0, nqb, warp & 3, lane);
+        pipe_dq_role(p, smem, b, abort_flag, tmem, warp & 3, lane);
     } else if (warp == 1) {
-        if (lane == 0 && nqb > 0) {
-            pipe_mma(p, smem, b, abort_flag, tmem, nqb);
+        if (lane == 0) {
+            pipe_mma(p, smem, b, abort_flag, tmem);
             tc_commit(b.done);  // every issued MMA finishes before tensor memory is released
             drain_wait(b.done, 0, p.status);
         }
         __syncwarp();
     } else {
-        if (lane == 0 && nqb > 0) pipe_producer(p, smem, b, abort_flag, bh, j, i0, nqb);
+        if (lane == 0) pipe_producer(p, smem, b, abort_flag);
         __syncwarp();
     }
 
@@ -941,7 +1064,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_pipe_kernel(const __grid_c
     }
 }
 
-cudaError_t launch_bwd_pipe(const BwdParams& p, cudaStream_t stream) {
+cudaError_t launch_bwd_pipe(const BwdParams& p, int sm_count, cudaStream_t stream) {
     using C = PCfg;
     const long long prep_warps = (long long)p.BH * p.nq_pad;
     bwd_prep_kernel<128><<<(unsigned)((prep_warps + 7) / 8), 256, 0, stream>>>(p);
@@ -949,7 +1072,9 @@ cudaError_t launch_bwd_pipe(const BwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    bwd_pipe_kernel<<<dim3((unsigned)p.n_kblocks, (unsigned)p.BH), kBwdThreads, C::SMEM_BYTES, stream>>>(p);
+    const long long n_units = (long long)p.BH * p.n_kblocks;
+    const int grid = (int)(n_units < sm_count ? n_units : sm_count);
+    bwd_pipe_kernel<<<grid, kBwdThreads, C::SMEM_BYTES, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long dq_warps = (long long)p.BH * p.Nq;
@@ -981,8 +1106,8 @@ size_t bwd_workspace_bytes(int BH, int Nq, int d) {
     return (size_t)BH * nq_pad * ((size_t)d + 2) * sizeof(float);
 }
 
-cudaError_t launch_bwd(int d, const BwdParams& p, cudaStream_t stream) {
-    if (d == 128) return launch_bwd_pipe(p, stream);
+cudaError_t launch_bwd(int d, const BwdParams& p, int sm_count, cudaStream_t stream) {
+    if (d == 128) return launch_bwd_pipe(p, sm_count, stream);
     if (d == 64) return launch_bwd_d<64>(p, stream);
     return cudaErrorInvalidValue;
 }

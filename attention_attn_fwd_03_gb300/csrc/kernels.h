@@ -178,7 +178,8 @@ constexpr int kBwdThreads = 320;  // TMA warp, MMA warp, dS warpgroup, dQ warpgr
 constexpr int bwd_q_rows(int d) { return d == 128 ? 64 : 128; }
 
 size_t bwd_workspace_bytes(int BH, int Nq, int d);
-cudaError_t launch_bwd(int d, const BwdParams& p, cudaStream_t stream);
+// sm_count: the persistent d = 128 kernel runs one CTA per SM (at most one per unit).
+cudaError_t launch_bwd(int d, const BwdParams& p, int sm_count, cudaStream_t stream);
 
 }  // namespace attn
 

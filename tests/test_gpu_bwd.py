@@ -58,6 +58,8 @@ def _check(B, H, Nq, Nk, d, causal, seed, heads=None):
     (1, 3, 40, 300, 128),    # fewer queries than one 64-row block (d = 128 runs 64-query blocks)
     (1, 2, 65, 129, 128),    # one query past a 64-row block, one key past a 128-key block
     (2, 4, 1024, 1024, 128),
+    (2, 24, 700, 700, 128),  # more (head, key block) units than SMs: causal CTAs loop over units
+    (1, 40, 333, 520, 128),
 ])
 def test_bwd(B, H, Nq, Nk, d, causal):
     _check(B, H, Nq, Nk, d, causal, seed=B * 100 + Nq + d)
