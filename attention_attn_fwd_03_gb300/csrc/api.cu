@@ -524,6 +524,7 @@ attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_c
     if (pl.n_splits > 1) {
         p.part_o = reinterpret_cast<float*>(ws + pl.part_o_offset);
         p.part_ml = reinterpret_cast<float*>(ws + pl.part_ml_offset);
+        if (pl.whole_offset != 0) p.whole = reinterpret_cast<int*>(ws + pl.whole_offset);
     }
     p.status = ds->status;
     p.B = B;
@@ -546,6 +547,7 @@ attn_status_t attn_paged_fwd(const void* q, const void* k_cache, const void* v_c
     p.q_tile_bytes = (uint32_t)(d / 64) * (uint32_t)(pl.G * pl.T) * 128u;
     p.c_scale = scale * 1.4426950408889634f;
     const int grid = pl.n_units < ds->sm_count ? (int)pl.n_units : ds->sm_count;  // persistent: one CTA per SM
+    p.n_ctas = grid;
     return from_cuda(launch_paged(d, p, grid, static_cast<cudaStream_t>(stream)));
 }
 
@@ -606,6 +608,7 @@ attn_status_t attn_varlen_fwd(const void* q, const void* k, const void* v, const
     if (pl.n_splits > 1) {
         p.part_o = reinterpret_cast<float*>(ws + pl.part_o_offset);
         p.part_ml = reinterpret_cast<float*>(ws + pl.part_ml_offset);
+        if (pl.whole_offset != 0) p.whole = reinterpret_cast<int*>(ws + pl.whole_offset);
     }
     p.status = ds->status;
     p.B = B;
@@ -628,6 +631,7 @@ attn_status_t attn_varlen_fwd(const void* q, const void* k, const void* v, const
     p.q_tile_bytes = (uint32_t)(d / 64) * (uint32_t)(pl.G * pl.T) * 128u;
     p.c_scale = scale * 1.4426950408889634f;
     const int grid = pl.n_units < ds->sm_count ? (int)pl.n_units : ds->sm_count;  // persistent: one CTA per SM
+    p.n_ctas = grid;
     return from_cuda(launch_paged(d, p, grid, static_cast<cudaStream_t>(stream)));
 }
 

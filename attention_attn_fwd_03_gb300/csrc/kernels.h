@@ -113,6 +113,7 @@ struct PagedParams {
     float* part_ml;              // [total_q * H, n_splits, 2] (m in log2 units, l)
     unsigned* status;
     int* sched;                  // [0] fetch counter, [1] list length (written by the schedule pass)
+    int* whole;                  // [B] or nullptr: 1 where the request's units cover all its keys (no merge)
     int4* sched_list;            // [n_units] units with work: (unit, q_start, q_len, kv_len)
     int B, H, H_kv, G, T;        // T = tokens per query tile
     int total_q, max_q_len, n_qt;
@@ -123,6 +124,7 @@ struct PagedParams {
     int n_units;                 // B * H_kv * n_qt * n_splits
     uint32_t q_tile_bytes;       // bytes one Q tile load delivers
     float c_scale;               // scale * log2(e)
+    int n_ctas;                  // CTAs of the paged kernel (its persistent grid)
 };
 
 constexpr int kPagedThreads = 192;  // TMA warp + MMA warp + one softmax warpgroup
@@ -133,6 +135,7 @@ struct PagedPlan {
     long long n_units;
     size_t list_offset;                  // byte offset of the unit list (after the 256-byte header)
     size_t part_o_bytes, part_ml_bytes;  // 0 when every unit covers all of its keys
+    size_t whole_offset;                 // byte offset of the per-request whole flags, 0: none
     size_t part_o_offset, part_ml_offset;
     size_t workspace_bytes;              // header + list + partials
 };

@@ -169,6 +169,17 @@ __device__ __forceinline__ void unit_tile(const PagedParams& p, int u, PUnit& g)
     g.nb = max(0, min(p.split_blocks, nb_all - g.kb0));
 }
 
+// A listed unit id with this bit set covers all of its request's KV blocks
+// (the request is not split: its unit writes O and the LSE itself).
+constexpr int kWholeBit = 1 << 30;
+
+// A whole request's unit: every KV block of its tile, no split.
+__device__ __forceinline__ void make_whole(const PagedParams& p, PUnit& g) {
+    g.split = -1;
+    g.kb0 = 0;
+    g.nb = g.nt > 0 ? tile_kv_blocks(p, g.q_len, g.kv_len, g.t0 + g.nt - 1) : 0;
+}
+
 __device__ __forceinline__ PUnit paged_unit(const PagedParams& p, int u) {
     PUnit g;
     request_extent(p, (u / p.H_kv) % p.B, g);
@@ -252,7 +263,7 @@ __device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& 
         cur.y = __shfl_sync(0xffffffffu, next.y, 0);
         cur.z = __shfl_sync(0xffffffffu, next.z, 0);
         cur.w = __shfl_sync(0xffffffffu, next.w, 0);
-        const int u = cur.x;
+        const int u = cur.x < 0 ? -1 : (cur.x & ~kWholeBit);
         const bool more = u >= 0;
         if (more && lane == 0) {
             const int k = (int)gridDim.x + atomicAdd(p.sched, 1);
@@ -265,6 +276,7 @@ __device__ void producer_role(const PagedParams& p, uint8_t* smem, const PBars& 
             g.kv_len = cur.w;
             g.bad = false;
             unit_tile(p, u, g);
+            if (cur.x & kWholeBit) make_whole(p, g);
         }
         // publish the unit (or the end mark) to the MMA issuer and the softmax warps
         if (lane == 0) {
@@ -458,7 +470,7 @@ __device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b
         const int head = g.kvh * p.G + gh;
         const size_t grow = (size_t)(g.q_start + g.t0 + (row_ok ? tr : 0)) * p.H + head;  // output row
         if (g.nb == 0) {  // no visible key: O = 0, LSE = -inf (split partials: the merge sees no split)
-            if (p.n_splits == 1 && g.split == 0 && row_ok) {
+            if ((p.n_splits == 1 || g.split < 0) && row_ok) {
                 uint16_t* dst = p.o + grow * D;
 #pragma unroll
                 for (int c = 0; c < D; c += 8) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
@@ -596,7 +608,7 @@ __device__ void softmax_role(const PagedParams& p, uint8_t* smem, const PBars& b
         tc_fence_before();
         bar_arrive(b.o_empty);
         const float m_use = (m == -INFINITY) ? 0.f : m;
-        if (p.n_splits == 1) {
+        if (p.n_splits == 1 || g.split < 0) {
             if (!row_ok) continue;
             const float inv = (l > 0.f) ? 1.f / l : 0.f;
             uint16_t* dst = p.o + grow * D;
@@ -726,10 +738,14 @@ constexpr int kCachedReqs = 2048;
 __global__ void __launch_bounds__(1024) paged_schedule_kernel(const PagedParams p) {
     __shared__ int s_qstart[kCachedReqs], s_qlen[kCachedReqs], s_kvlen[kCachedReqs];
     __shared__ int s_bucket[kBuckets];
+    __shared__ unsigned long long s_work;
     griddep_launch_dependents();  // the paged kernel may start its prologue now
     const int t = threadIdx.x, lane = t & 31;
     const bool cached = p.B <= kCachedReqs;
+    if (t == 0) s_work = 0ull;
+    __syncthreads();
     bool bad = false;
+    unsigned long long work = 0;  // KV blocks of this thread's requests (one tile each when whole is set)
     for (int r = t; r < p.B; r += 1024) {
         PUnit g;
         request_extent(p, r, g);
@@ -739,10 +755,36 @@ __global__ void __launch_bounds__(1024) paged_schedule_kernel(const PagedParams 
             s_qlen[r] = g.q_len;
             s_kvlen[r] = g.kv_len;
         }
+        if (p.whole != nullptr && g.q_len > 0) work += (unsigned long long)tile_kv_blocks(p, g.q_len, g.kv_len, min(p.T, g.q_len) - 1);
     }
     if (bad) atomicOr(p.status, 1u << kStatusDeviceData);
     if (t < kBuckets) s_bucket[t] = 0;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) work += __shfl_xor_sync(0xffffffffu, work, o);
+    if (lane == 0 && work) atomicAdd(&s_work, work);
     __syncthreads();
+    // Decode-like launches (one query tile per request): a request whose KV
+    // blocks are at most half of a CTA's share of the launch (or one split)
+    // runs as one unit -- no partials, no merge -- and only the longer ones
+    // are split, so that the work still balances over the CTAs.
+    const long long share = (long long)(s_work * (unsigned long long)p.H_kv / (unsigned long long)(2 * p.n_ctas));
+    const long long thresh = share > p.split_blocks ? share : p.split_blocks;
+    auto is_whole = [&](const PUnit& g) {
+        return p.whole != nullptr && g.q_len > 0 && tile_kv_blocks(p, g.q_len, g.kv_len, min(p.T, g.q_len) - 1) <= thresh;
+    };
+    if (p.whole != nullptr) {
+        for (int r = t; r < p.B; r += 1024) {
+            PUnit g;
+            if (cached) {
+                g.q_start = s_qstart[r];
+                g.q_len = s_qlen[r];
+                g.kv_len = s_kvlen[r];
+            } else {
+                request_extent(p, r, g);
+            }
+            p.whole[r] = is_whole(g) ? 1 : 0;
+        }
+    }
     // group gi -> its first unit gi * H_kv, the request's extent, and its
     // work: KV blocks (0 for a unit that only zeroes rows), -1 for none
     auto group = [&](int gi, PUnit& g) {
@@ -755,6 +797,11 @@ __global__ void __launch_bounds__(1024) paged_schedule_kernel(const PagedParams 
             request_extent(p, r, g);
         }
         unit_tile(p, gi * p.H_kv, g);
+        if (is_whole(g)) {  // split 0 only, over all the tile's blocks
+            if (g.split > 0) return -1;
+            make_whole(p, g);
+            return g.nb > 0 ? g.nb : (g.nt > 0 ? 0 : -1);
+        }
         if (g.nb > 0) return g.nb;
         return (p.n_splits == 1 && g.nt > 0) ? 0 : -1;
     };
@@ -798,9 +845,10 @@ __global__ void __launch_bounds__(1024) paged_schedule_kernel(const PagedParams 
         PUnit g;
         const int w = gi < n_groups ? group(gi, g) : -1;
         const int pos = reserve(w >= 0 ? bucket(w) : 0, w >= 0);
+        const int flag = (w >= 0 && g.split < 0) ? kWholeBit : 0;
         if (w >= 0)
             for (int h = 0; h < p.H_kv; ++h)
-                p.sched_list[pos + h] = make_int4(gi * p.H_kv + h, g.q_start, g.q_len, g.kv_len);
+                p.sched_list[pos + h] = make_int4((gi * p.H_kv + h) | flag, g.q_start, g.q_len, g.kv_len);
     }
     if (t == 0) p.sched[0] = 0;
 }
@@ -833,6 +881,7 @@ __global__ void __launch_bounds__(512) paged_merge_kernel(const PagedParams p) {
     request_extent(p, r, g);
     const int t = tok - g.q_start;
     if (t < 0 || t >= g.q_len) return;  // token not owned by a valid request (reported by the main kernel)
+    if (p.whole != nullptr && __ldg(p.whole + r)) return;  // written by its unit
     const int t0 = (t / p.T) * p.T;
     const int nb = tile_kv_blocks(p, g.q_len, g.kv_len, min(t0 + p.T, g.q_len) - 1);
     const int ns = (nb + p.split_blocks - 1) / p.split_blocks;
@@ -967,6 +1016,12 @@ PagedPlan paged_plan(int total_q, int max_q_len, int B, int H, int H_kv, int d, 
         pl.workspace_bytes += (pl.part_o_bytes + 255) / 256 * 256;
         pl.part_ml_offset = pl.workspace_bytes;
         pl.workspace_bytes += pl.part_ml_bytes;
+        // decode-like launches: per-request flags for requests run unsplit
+        if (pl.n_qt == 1 && pl.n_units < (1LL << 30)) {
+            pl.workspace_bytes = (pl.workspace_bytes + 255) / 256 * 256;
+            pl.whole_offset = pl.workspace_bytes;
+            pl.workspace_bytes += (size_t)B * sizeof(int);
+        }
     }
     return pl;
 }

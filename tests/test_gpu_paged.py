@@ -60,6 +60,8 @@ def _ref(p, scale, causal=False, chunks=False):
     (2, 24, 8, 128, 1024, 2, 1, 2048),    # G = 3: 126 of 128 tile rows used
     (2, 128, 1, 128, 64, 4, 1, 256),      # G = 128: the whole tile is one token
     (3, 4, 4, 128, 32, 8, 1, 256),        # G = 1 (multi-head)
+    (12, 32, 8, 128, 64, 100, 1, 6000),   # lengths 1..6000: short requests run unsplit, long ones split
+    (40, 16, 4, 64, 16, 300, 0, 4800),    # many streams, empty requests possible
 ])
 def test_grouped_decode(B, H, H_kv, d, page, max_pages, lo, hi):
     p = inputs.paged_kv(B=B, H=H, d=d, page_size=page, max_pages=max_pages, num_pages=B * max_pages + 7,
