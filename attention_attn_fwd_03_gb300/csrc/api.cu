@@ -646,6 +646,8 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return ATTN_ERR_INVALID_ARG;
     if ((long long)B * H > 65535) return ATTN_ERR_UNSUPPORTED;  // grid.y holds batch * heads
+    // the d = 128 kernel counts (batch*head, 128-key block) units in 32 bits
+    if ((long long)B * H * (((long long)Nk + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
     if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||

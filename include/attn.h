@@ -244,7 +244,8 @@ size_t attn_bwd_workspace_size(int B, int H, int Nq, int d);
  *   keys no query sees get dK = dV = 0.
  *   workspace: attn_bwd_workspace_size(B, H, Nq, d) bytes, caller-owned,
  *   16-byte aligned, no initialisation needed.
- *   d in {64, 128}; B * H <= 65535.  Errors as attn_fwd, plus
+ *   d in {64, 128}; B * H <= 65535 and B * H * ceil(Nk / 128) < 2^31
+ *   (else ATTN_ERR_UNSUPPORTED).  Errors as attn_fwd, plus
  *   ATTN_ERR_WORKSPACE. */
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                        const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,

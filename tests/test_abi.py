@@ -183,6 +183,8 @@ def test_bwd_validation(L):
     assert attn.attn_bwd(**dict(base, d=96)) == attn.ATTN_ERR_UNSUPPORTED
     assert attn.attn_bwd(**dict(base, workspace_bytes=ws - 4)) == attn.ATTN_ERR_WORKSPACE
     assert attn.attn_bwd(**dict(base, causal=3)) == attn.ATTN_ERR_INVALID_ARG
+    # (batch*head, 128-key block) units past 2^31: refused before anything is enqueued
+    assert attn.attn_bwd(**dict(base, B=16, H=64, Nk=2 ** 30)) == attn.ATTN_ERR_UNSUPPORTED
 
 
 def test_fwd_host_workspace_and_validation(L):
