@@ -172,6 +172,22 @@ def test_varlen_fwd_validation(L):
     assert attn.attn_varlen_fwd(**dict(base, cu_seqlens_q=FAKE + 2)) == attn.ATTN_ERR_INVALID_ARG
 
 
+def test_paged_workspace_layout(L):
+    """attn_paged_fwd's workspace: a 256-byte header, the unit list (16 bytes per unit, rounded to
+    256), then for split launches the fp32 partial O and (m, l) per row and split, and for
+    decode-like split launches one int per request (requests run unsplit)."""
+    # 64 requests x 32 heads over 8 KV heads, one token each, up to 128 pages of 64 tokens:
+    # 64 KV blocks per request in splits of 8 -> 8 splits, 64 * 8 * 8 units
+    units = 64 * 8 * 8
+    size = 256 + (units * 16 + 255) // 256 * 256
+    size += 64 * 32 * 8 * 128 * 4          # partial O
+    size += 64 * 32 * 8 * 2 * 4            # partial (m, l)
+    size = (size + 255) // 256 * 256 + 64 * 4  # per-request flags
+    assert attn.attn_paged_fwd_workspace_size(64, 64, 1, 32, 8, 128, 64, 128) == size
+    # 8 KV blocks at most: one split, no partials, no flags
+    assert attn.attn_paged_fwd_workspace_size(4, 4, 1, 8, 2, 128, 64, 16) == 256 + 256
+
+
 def test_bwd_validation(L):
     ws = attn.attn_bwd_workspace_size(2, 4, 300, 128)
     assert ws == 2 * 4 * 384 * 130 * 4  # dQ accumulator + two row vectors, rows padded to 128
